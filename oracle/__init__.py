@@ -1,0 +1,224 @@
+"""Python binding of the fp64 CPU attention oracle (``attn_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the test suite, the package smoke check and the
+benchmark's CPU-baseline leg are the only callers.  The CUDA library never
+imports this module and this module never imports the CUDA library.
+
+``build()`` compiles ``attn_oracle.c`` with the system C compiler into
+``oracle/_build/libattn_oracle.so`` (OpenMP when available, no fast-math).
+All entry points take and return float64 numpy arrays; 16-bit inputs are
+widened exactly by ``to_f64``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libattn_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+
+
+def build(force: bool = False, src: str | None = None, out: str | None = None) -> str:
+    """Compile the oracle shared library; returns its path.
+
+    ``src``/``out`` let a test compile a modified copy of the source elsewhere.
+    """
+    src = src or _SRC
+    out = out or _LIB_PATH
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", src, "-o", out + ".tmp", "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(out + ".tmp", out)
+    return out
+
+
+def _bind(lib):
+    lib.oracle_set_threads.argtypes = [ctypes.c_int]
+    lib.oracle_set_threads.restype = ctypes.c_int
+    lib.oracle_has_openmp.argtypes = []
+    lib.oracle_has_openmp.restype = ctypes.c_int
+    lib.oracle_attn_full.argtypes = [_dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_double, _dp, _dp]
+    lib.oracle_attn_full.restype = ctypes.c_int
+    lib.oracle_attn_rows.argtypes = [_dp, _i64p, _i64p, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_double, _dp, _dp]
+    lib.oracle_attn_rows.restype = ctypes.c_int
+    lib.oracle_attn_tiled.argtypes = [_dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int, _dp, _dp]
+    lib.oracle_attn_tiled.restype = ctypes.c_int
+    lib.oracle_attn_split_partials.argtypes = [_dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                                               ctypes.c_long, _dp, _dp]
+    lib.oracle_attn_split_partials.restype = ctypes.c_int
+    lib.oracle_combine.argtypes = [_dp, _dp, ctypes.c_int, ctypes.c_long, ctypes.c_int, _dp, _dp]
+    lib.oracle_combine.restype = ctypes.c_int
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building if needed) the oracle library. A ``path`` loads a separate copy."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def set_threads(n: int) -> int:
+    return load().oracle_set_threads(int(n))
+
+
+def has_openmp() -> bool:
+    return bool(load().oracle_has_openmp())
+
+
+def to_f64(x) -> np.ndarray:
+    """Exact widening of a torch tensor (any float dtype) or array to contiguous float64 numpy."""
+    try:
+        import torch
+
+        if isinstance(x, torch.Tensor):
+            return np.ascontiguousarray(x.detach().to("cpu").to(torch.float64).numpy())
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _p(a: np.ndarray):
+    assert a.dtype == np.float64 and a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(_dp)
+
+
+def attention(q, k, v, causal: bool, scale: float, lib=None):
+    """Exact attention.  q: [..., Nq, d], k, v: [..., Nk, d] -> (O [..., Nq, d], LSE [..., Nq])."""
+    lib = lib or load()
+    q, k, v = to_f64(q), to_f64(k), to_f64(v)
+    lead = q.shape[:-2]
+    Nq, d = q.shape[-2:]
+    Nk = k.shape[-2]
+    BH = int(np.prod(lead)) if lead else 1
+    o = np.zeros(q.shape, dtype=np.float64)
+    lse = np.zeros(lead + (Nq,), dtype=np.float64)
+    rc = lib.oracle_attn_full(_p(q), _p(k), _p(v), BH, Nq, Nk, d, int(bool(causal)), float(scale), _p(o), _p(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_full failed ({rc})")
+    return o, lse
+
+
+def attention_tiled(q, k, v, causal: bool, scale: float, Br: int, Bc: int, lib=None):
+    """The page-4 online-softmax loop in fp64 (for the tiled == full invariant)."""
+    lib = lib or load()
+    q, k, v = to_f64(q), to_f64(k), to_f64(v)
+    lead = q.shape[:-2]
+    Nq, d = q.shape[-2:]
+    Nk = k.shape[-2]
+    BH = int(np.prod(lead)) if lead else 1
+    o = np.zeros(q.shape, dtype=np.float64)
+    lse = np.zeros(lead + (Nq,), dtype=np.float64)
+    rc = lib.oracle_attn_tiled(_p(q), _p(k), _p(v), BH, Nq, Nk, d, int(bool(causal)), float(scale),
+                               int(Br), int(Bc), _p(o), _p(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_tiled failed ({rc})")
+    return o, lse
+
+
+def split_partials(q, k, v, causal: bool, scale: float, num_splits: int, split_len: int, lib=None):
+    """Per-split normalised partials: (O_s [S, ..., Nq, d], LSE_s [S, ..., Nq])."""
+    lib = lib or load()
+    q, k, v = to_f64(q), to_f64(k), to_f64(v)
+    lead = q.shape[:-2]
+    Nq, d = q.shape[-2:]
+    Nk = k.shape[-2]
+    BH = int(np.prod(lead)) if lead else 1
+    o = np.zeros((num_splits,) + q.shape, dtype=np.float64)
+    lse = np.zeros((num_splits,) + lead + (Nq,), dtype=np.float64)
+    rc = lib.oracle_attn_split_partials(_p(q), _p(k), _p(v), BH, Nq, Nk, d, int(bool(causal)), float(scale),
+                                        int(num_splits), int(split_len), _p(o), _p(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_split_partials failed ({rc})")
+    return o, lse
+
+
+def combine(o_part, lse_part, lib=None):
+    """LSE-weighted merge.  o_part: [S, ..., d], lse_part: [S, ...] -> (O [..., d], LSE [...])."""
+    lib = lib or load()
+    o_part, lse_part = to_f64(o_part), to_f64(lse_part)
+    S = o_part.shape[0]
+    d = o_part.shape[-1]
+    rows = int(np.prod(o_part.shape[1:-1])) if o_part.ndim > 2 else 1
+    o = np.zeros(o_part.shape[1:], dtype=np.float64)
+    lse = np.zeros(lse_part.shape[1:], dtype=np.float64)
+    rc = lib.oracle_combine(_p(o_part), _p(lse_part), S, rows, d, _p(o), _p(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_combine failed ({rc})")
+    return o, lse
+
+
+def attention_rows(q_rows, row_index, kv_slot, k, v, Nq: int, causal: bool, scale: float, lib=None):
+    """Selected rows.  q_rows: [n, d]; row_index, kv_slot: [n] ints; k, v: [slots, Nk, d]."""
+    lib = lib or load()
+    q_rows, k, v = to_f64(q_rows), to_f64(k), to_f64(v)
+    ri = np.ascontiguousarray(np.asarray(row_index, dtype=np.int64))
+    ks = np.ascontiguousarray(np.asarray(kv_slot, dtype=np.int64))
+    n, d = q_rows.shape
+    Nk = k.shape[-2]
+    o = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    rc = lib.oracle_attn_rows(_p(q_rows), ri.ctypes.data_as(_i64p), ks.ctypes.data_as(_i64p), _p(k), _p(v),
+                              n, int(Nq), Nk, d, int(bool(causal)), float(scale), _p(o), _p(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_rows failed ({rc})")
+    return o, lse
+
+
+def sampled_rows(q, k, v, pairs, causal: bool, scale: float, heads_per_batch: int = 16):
+    """Oracle values for the (bh, row) pairs of ``[B, H, N, d]`` tensors (any device).
+
+    Only the heads that appear in ``pairs`` are copied to the host, a few at a
+    time, so that large workloads stay within host memory.
+    Returns (O [n, d], LSE [n]) in the order of ``pairs``.
+    """
+    d = q.shape[-1]
+    Nq = q.shape[-2]
+    qf = q.reshape(-1, Nq, d)
+    kf = k.reshape(-1, k.shape[-2], d)
+    vf = v.reshape(-1, v.shape[-2], d)
+    by_bh: dict[int, list[int]] = {}
+    for n, (bh, _r) in enumerate(pairs):
+        by_bh.setdefault(int(bh), []).append(n)
+    o = np.zeros((len(pairs), d))
+    lse = np.zeros((len(pairs),))
+    bhs = sorted(by_bh)
+    for s in range(0, len(bhs), heads_per_batch):
+        group = bhs[s:s + heads_per_batch]
+        kk = np.stack([to_f64(kf[bh]) for bh in group])
+        vv = np.stack([to_f64(vf[bh]) for bh in group])
+        idx, rows, slots, qr = [], [], [], []
+        for slot, bh in enumerate(group):
+            for n in by_bh[bh]:
+                idx.append(n)
+                rows.append(pairs[n][1])
+                slots.append(slot)
+                qr.append(to_f64(qf[bh, pairs[n][1]]))
+        oo, ll = attention_rows(np.stack(qr), rows, slots, kk, vv, Nq, causal, scale)
+        o[idx] = oo
+        lse[idx] = ll
+    return o, lse
