@@ -1,0 +1,441 @@
+#!/usr/bin/env python
+"""Benchmark of the attention forward hot path on GB300; prints one JSON line.
+
+Default workload: causal attention forward, B=2, H=32, Nq=Nk=8192, d=128,
+bf16 inputs drawn N(0,1) from fixed seeds, scale 1/sqrt(d).  The headline
+`value` is its throughput in TFLOP/s, counting 4*B*H*Nq*Nk*d FLOPs halved for
+causal, timed with CUDA events around every fa_fwd launch on the launching
+stream, with the L2 cache flushed (a 256 MiB write) before each timed launch.
+The split-KV decode path (B=32, H=32, Nq=1, Nk=16384, d=128, bf16, 16 splits)
+is timed the same way and reported under "decode" in GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fa|reference]
+
+--impl reference times the fp64 CPU oracle (the reference arm of this
+benchmark) on a bounded sample of query rows of the same workload.
+Under torchrun every rank runs an independent replica; rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import attn_inputs  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (fraction of GB300 dense BF16 peak); decode GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_setup(n_gpus: int):
+    """(rank, world, local_rank); initialises torch.distributed when launched by torchrun."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest value of x over all ranks (replica timings: the slowest rank decides)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi while the timed region runs."""
+
+    QUERY = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.rows = []
+        self.proc = None
+        self.thread = None
+        self.active = False
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and self.uuid not in parts[0] and parts[0] not in self.uuid:
+                continue
+            self.rows.append((time.time(), self.active, parts))
+
+    def mark(self, active: bool):
+        self.active = active
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        rows = [r for r in self.rows if r[1]] or self.rows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[2][1]) for r in rows if num(r[2][1]) is not None]
+        smax = [num(r[2][2]) for r in rows if num(r[2][2]) is not None]
+        power = [num(r[2][3]) for r in rows if num(r[2][3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[2][5:9]) if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": reasons, "samples": len(rows)}
+
+
+def device_uuid():
+    try:
+        u = torch.cuda.get_device_properties(torch.cuda.current_device()).uuid
+        return "GPU-" + str(u)
+    except Exception:  # noqa: BLE001
+        return None
+
+
+def time_calls(fn, steps: int, warmup: int, flush: torch.Tensor | None):
+    """Per-call device milliseconds of fn() with CUDA events on the current stream."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in evs:
+        if flush is not None:
+            flush.fill_(1)  # evicts the previous call's lines from L2
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def oracle_rate(w: attn_inputs.Workload, q, k, v, seconds: float, threads: int, seed: int = 0):
+    """Time the fp64 oracle on sampled rows for about `seconds`; returns (TFLOP/s, rows, elapsed)."""
+    import oracle
+
+    oracle.set_threads(threads)
+
+    def flops_of(pairs):
+        tot = 0.0
+        for _bh, i in pairs:
+            vis = min(w.Nk, i + (w.Nk - w.Nq) + 1) if w.causal else w.Nk
+            tot += 4.0 * w.d * max(vis, 0)
+        return tot
+
+    BH = w.B * w.H
+    n = max(threads, 8)
+    t_total, f_total, rows_total = 0.0, 0.0, 0
+    rnd = seed
+    while True:
+        pairs = attn_inputs.sample_rows(w.Nq, BH, n, seed=rnd)
+        rnd += 1
+        t0 = time.perf_counter()
+        oracle.sampled_rows(q, k, v, pairs, w.causal, w.scale)
+        dt = time.perf_counter() - t0
+        t_total += dt
+        f_total += flops_of(pairs)
+        rows_total += len(pairs)
+        if t_total >= seconds:
+            break
+        n = int(min(max(n * 2, n * (seconds - t_total) / max(dt, 1e-3)), 1 << 16))
+    return f_total / t_total / 1e12, rows_total, t_total
+
+
+def oracle_decode_rate(w: attn_inputs.Workload, q, k, v, seconds: float, threads: int):
+    """Oracle GB/s on sampled (b, h) rows of the decode workload (bytes of K and V touched)."""
+    import oracle
+
+    oracle.set_threads(threads)
+    BH = w.B * w.H
+    n, t_total, b_total, rows = 4, 0.0, 0.0, 0
+    rnd = 0
+    while True:
+        pairs = attn_inputs.sample_rows(1, BH, n, seed=rnd)
+        rnd += 1
+        t0 = time.perf_counter()
+        oracle.sampled_rows(q, k, v, pairs, False, w.scale)
+        dt = time.perf_counter() - t0
+        t_total += dt
+        b_total += len(pairs) * (2 * w.Nk * w.d * 2 + 2 * w.d * 2 + 4)
+        rows += len(pairs)
+        if t_total >= seconds:
+            break
+        n = int(min(max(n * 2, n * (seconds - t_total) / max(dt, 1e-3)), BH))
+    return b_total / t_total / 1e9, rows, t_total
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args, rank, world):
+    """The fp64 CPU oracle as the reference arm, on this arm's workload and metric."""
+    if rank != 0:
+        return
+    w = attn_inputs.WORKLOADS[args.workload]
+    threads = os.cpu_count() or 1
+    q, k, v = attn_inputs.make_workload(w, "cpu")
+    import oracle
+
+    oracle.build()
+    budget = max(0.5, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup):
+        oracle_rate(w, q, k, v, budget * 0.25, threads, seed=10_000 + i)
+    rates, times = [], []
+    for i in range(args.steps):
+        r, rows, dt = oracle_rate(w, q, k, v, budget, threads, seed=20_000 + i)
+        rates.append(r)
+        times.append(dt)
+    value = statistics.median(rates)
+    sample = (f"each step: the fp64 oracle on about {budget:.1f} s of uniformly sampled query rows "
+              f"(full key range per row) of {w.name}")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * statistics.median(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, flushed=False),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w: attn_inputs.Workload, flushed=True, parallelism="replicas"):
+    return {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "dtype": w.dtype,
+            "causal": w.causal, "scale": "1/sqrt(d)",
+            "l2": "flushed before every timed launch (256 MiB write)" if flushed else "n/a",
+            "parallelism": parallelism}
+
+
+def run_fa(args, rank, world, local):
+    import exact_attention_forward_03_gb300 as fa
+    from exact_attention_forward_03_gb300 import build
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU; the CPU arm is --impl reference")
+    build.build()
+    fa.load_library()
+    peaks, peak_src = load_peaks()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = attn_inputs.WORKLOADS[args.workload]
+    q, k, v = attn_inputs.make_workload(w, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    sampler = ClockSampler(device_uuid())
+    sampler.start()
+    time.sleep(0.3)
+
+    def call():
+        fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
+
+    # ---- timed region: fused forward
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.mark(True)
+    t_wall0 = time.perf_counter()
+    ms = time_calls(call, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall0
+    barrier(world)
+    ms_mean = statistics.mean(ms)
+    ms_max = max_over_ranks(ms_mean, world)
+    status = fa.get_device_status()
+    if status != fa.FA_OK:
+        raise RuntimeError(f"device status {status} after the timed region")
+    flops = w.flops()
+    value = sum_over_ranks(flops, world) / (ms_max * 1e-3) / 1e12
+    achieved = flops / (ms_mean * 1e-3) / 1e12
+    launches = args.steps
+
+    # ---- decode (split-KV + combine)
+    decode = None
+    if not args.no_decode:
+        wd = attn_inputs.WORKLOADS[args.decode_workload]
+        del q, k, v
+        torch.cuda.empty_cache()
+        dq, dk, dv = attn_inputs.make_workload(wd, dev)
+        do = torch.empty_like(dq)
+        dl = torch.empty((wd.B, wd.H, wd.Nq), dtype=torch.float32, device=dev)
+        ws = fa.splitkv_workspace(dq, dk, args.decode_splits)
+
+        def dcall():
+            fa.fwd_splitkv(dq, dk, dv, causal=False, scale=wd.scale, num_splits=args.decode_splits, workspace=ws,
+                           out=do, lse=dl)
+
+        dms = time_calls(dcall, args.steps, args.warmup, flush)
+        launches += 2 * args.steps
+        dmean = statistics.mean(dms)
+        dbytes = wd.compulsory_bytes()
+        gbs = dbytes / (dmean * 1e-3) / 1e9
+        part_bytes = 2 * args.decode_splits * wd.B * wd.H * wd.Nq * (wd.d + 1) * 4
+        decode = {"workload": wd.name, "num_splits": args.decode_splits, "ms_per_call": dmean,
+                  "value": sum_over_ranks(dbytes, world) / (max_over_ranks(dmean, world) * 1e-3) / 1e9,
+                  "unit": "GB/s",
+                  "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                               "note": f"compulsory bytes (Q, K, V read, O, LSE written) per call; peak {peak_src}; "
+                                       "split-partial traffic (written and re-read by the combine) excluded: "
+                                       f"{part_bytes} bytes per call"}}
+        del dq, dk, dv, ws
+        torch.cuda.empty_cache()
+        q, k, v = attn_inputs.make_workload(w, dev)
+    sampler.mark(False)
+    sampler.stop()
+    clocks = sampler.summary()
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        qh, kh, vh = (t.to("cpu").pin_memory() for t in (q, k, v))
+        oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def ecall():
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            fa.fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=o, lse=lse)
+            oh.copy_(o, non_blocking=True)
+            lh.copy_(lse, non_blocking=True)
+
+        esteps = max(3, min(args.steps, 20))
+        ems = time_calls(ecall, esteps, max(1, min(args.warmup, 3)), None)
+        launches += esteps
+        emean = max_over_ranks(statistics.mean(ems), world)
+        e2e = {"value": sum_over_ranks(flops, world) / (emean * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
+               "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * 4,
+               "ms_per_step": emean, "steps": esteps}
+
+    # ---- the oracle on this machine's host cores (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        rate, rows, secs = oracle_rate(w, q, k, v, args.cpu_seconds, threads)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{rows} uniformly sampled query rows of {w.name} (full key range each), {secs:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f16", "data": "synthetic",
+        "config": workload_config(w),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"],
+                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                     "traffic": args.traffic, "peak_source": peak_src,
+                     "kernel": "fa_fwd_kernel<128,bf16>", "flops_per_launch": flops},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "decode": decode,
+        "wall_s_fwd_timed": wall, "ms_fwd_min": min(ms), "ms_fwd_median": statistics.median(ms),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["fa", "reference"], default="fa")
+    ap.add_argument("--workload", default="b2h32_n8192_d128_bf16_causal", choices=sorted(attn_inputs.WORKLOADS))
+    ap.add_argument("--decode-workload", default="decode_b32h32_nk16384_d128_bf16")
+    ap.add_argument("--decode-splits", type=int, default=16)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the fused kernel from an ncu capture (reported as roofline.traffic)")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up calls, whatever was asked
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_fa(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,221 @@
+"""Exact attention forward for GB300 (sm_103a): a thin ctypes binding of libfa.so.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+only checks tensors, allocates outputs with torch when the caller passes none,
+and forwards raw pointers, sizes and the current CUDA stream to the C ABI
+declared in ``include/fa.h``.  There is no fallback: if ``libfa.so`` is not
+built or the tensors are not on a CUDA device, the calls raise.
+
+Functions (same names as the C ABI without the ``fa_`` prefix):
+    fwd(q, k, v, causal=False, scale=None, out=None, lse=None)            -> (o, lse)
+    fwd_splitkv(q, k, v, causal=False, scale=None, num_splits=0, ...)     -> (o, lse)
+    splitkv_combine(o_part, lse_part, out=None, lse=None, dtype=...)      -> (o, lse)
+    splitkv_num_splits, splitkv_split_len, splitkv_workspace_bytes,
+    get_device_status, status_string, version
+Tensors are ``[B, H, N, d]`` contiguous fp16 or bf16 on one CUDA device;
+``lse`` is ``[B, H, Nq]`` fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfa.so")
+
+FA_F16, FA_BF16 = 0, 1
+FA_OK = 0
+FA_ERR_INVALID_ARG = -1
+FA_ERR_UNSUPPORTED = -2
+FA_ERR_MISALIGNED = -3
+FA_ERR_WORKSPACE = -4
+FA_ERR_CUDA = -5
+FA_ERR_DEVICE_TIMEOUT = -6
+
+EXPORTS = ("fa_fwd", "fa_fwd_splitkv", "fa_splitkv_combine", "fa_splitkv_workspace_bytes",
+           "fa_splitkv_num_splits", "fa_splitkv_split_len", "fa_get_device_status", "fa_status_string",
+           "fa_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+        self.code = code
+
+
+def load_library(path: str | None = None):
+    """Load libfa.so (built by ``build.build()``) and declare its C signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is not built; run exact_attention_forward_03_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd.restype = i
+        lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, sz, vp]
+        lib.fa_fwd_splitkv.restype = i
+        lib.fa_splitkv_combine.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp]
+        lib.fa_splitkv_combine.restype = i
+        lib.fa_splitkv_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        lib.fa_splitkv_workspace_bytes.restype = sz
+        lib.fa_splitkv_num_splits.argtypes = [i, i, i, i, i]
+        lib.fa_splitkv_num_splits.restype = i
+        lib.fa_splitkv_split_len.argtypes = [i, i]
+        lib.fa_splitkv_split_len.restype = i
+        lib.fa_get_device_status.argtypes = [vp]
+        lib.fa_get_device_status.restype = i
+        lib.fa_status_string.argtypes = [i]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_version.argtypes = []
+        lib.fa_version.restype = i
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return load_library().fa_status_string(int(code)).decode()
+    except RuntimeError:
+        return f"status {code}"
+
+
+def version() -> int:
+    return load_library().fa_version()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return FA_F16
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    raise TypeError(f"dtype {t.dtype} not supported (fp16 or bf16)")
+
+
+def _stream_handle(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _check_qkv(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    B, H, Nq, d = q.shape
+    if k.shape[:2] != (B, H) or v.shape != k.shape or k.shape[3] != d:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    return B, H, Nq, k.shape[2], d
+
+
+def _outputs(q, out, lse, B, H, Nq, want_lse=True):
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must match q")
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    elif lse is not None and (lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor")
+    return out, lse
+
+
+def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, want_lse: bool = True,
+        stream=None):
+    """Fused attention forward through ``fa_fwd``.  Returns (o, lse)."""
+    B, H, Nq, Nk, d = _check_qkv(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out, lse = _outputs(q, out, lse, B, H, Nq, want_lse)
+    lib = load_library()
+    rc = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                    lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d, int(bool(causal)), scale,
+                    _dtype_code(q), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd")
+    return out, lse
+
+
+def splitkv_num_splits(B, H, Nq, Nk, d) -> int:
+    return load_library().fa_splitkv_num_splits(B, H, Nq, Nk, d)
+
+
+def splitkv_split_len(Nk, num_splits) -> int:
+    return load_library().fa_splitkv_split_len(Nk, num_splits)
+
+
+def splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits=0) -> int:
+    return load_library().fa_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits)
+
+
+def splitkv_workspace(q, k, num_splits=0):
+    """Allocate a workspace tensor for ``fwd_splitkv`` (torch allocator, 256-byte aligned)."""
+    B, H, Nq, d = q.shape
+    nbytes = splitkv_workspace_bytes(B, H, Nq, k.shape[2], d, num_splits)
+    if nbytes == 0:
+        raise ValueError("invalid sizes for a split-KV workspace")
+    return torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+
+
+def fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None, num_splits: int = 0, workspace=None,
+                out=None, lse=None, want_lse: bool = True, stream=None):
+    """Split-KV forward (partials + combine) through ``fa_fwd_splitkv``.  Returns (o, lse)."""
+    B, H, Nq, Nk, d = _check_qkv(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out, lse = _outputs(q, out, lse, B, H, Nq, want_lse)
+    if num_splits <= 0:
+        num_splits = splitkv_num_splits(B, H, Nq, Nk, d)
+    if workspace is None:
+        workspace = splitkv_workspace(q, k, num_splits)
+    lib = load_library()
+    rc = lib.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d, int(bool(causal)), scale,
+                            _dtype_code(q), int(num_splits), workspace.data_ptr(),
+                            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_splitkv")
+    return out, lse
+
+
+def workspace_views(workspace, B, H, Nq, d, num_splits):
+    """The (o_part [S, B, H, Nq, d], lse_part [S, B, H, Nq]) fp32 views of a split-KV workspace."""
+    rows = B * H * Nq
+    o_bytes = (num_splits * rows * d * 4 + 255) // 256 * 256
+    o_part = workspace[: num_splits * rows * d * 4].view(torch.float32).view(num_splits, B, H, Nq, d)
+    lse_part = workspace[o_bytes: o_bytes + num_splits * rows * 4].view(torch.float32).view(num_splits, B, H, Nq)
+    return o_part, lse_part
+
+
+def splitkv_combine(o_part, lse_part, dtype=torch.bfloat16, out=None, lse=None, stream=None):
+    """LSE-weighted merge of fp32 partials through ``fa_splitkv_combine``.  Returns (o, lse)."""
+    if o_part.dim() != 5 or lse_part.dim() != 4 or not o_part.is_contiguous() or not lse_part.is_contiguous():
+        raise ValueError("o_part must be [S, B, H, Nq, d] and lse_part [S, B, H, Nq], contiguous")
+    S, B, H, Nq, d = o_part.shape
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=dtype, device=o_part.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=o_part.device)
+    lib = load_library()
+    rc = lib.fa_splitkv_combine(o_part.data_ptr(), lse_part.data_ptr(), out.data_ptr(), lse.data_ptr(), S, B, H, Nq,
+                                d, _dtype_code(out), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_splitkv_combine")
+    return out, lse
+
+
+def get_device_status(stream=None) -> int:
+    """Synchronise the stream and return the library's device status (FA_OK, FA_ERR_DEVICE_TIMEOUT, ...)."""
+    return load_library().fa_get_device_status(_stream_handle(stream))

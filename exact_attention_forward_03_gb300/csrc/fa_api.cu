@@ -1,0 +1,253 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument checks, TMA
+// tensor-map encoding, split planning and kernel launches.  Host code only;
+// the kernels live in fa_fwd_sm103.cu and fa_splitkv.cu.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+
+// Per-device status word: kernels OR error bits into it (see kDevErrTimeout).
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int *status = nullptr;  // device address of g_status_word
+    int num_sms = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int dev_state(DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &st = g_dev[dev];
+    if (!st.ready) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return FA_ERR_CUDA;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FA_ERR_CUDA;
+        st.status = static_cast<int *>(p);
+        st.num_sms = sms;
+        st.ready = true;
+    }
+    if (g_encode == nullptr) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return FA_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    *out = &st;
+    return FA_OK;
+}
+
+// [BH][rows][d] 16-bit tensor, boxes of 64 columns (128 bytes) x box_rows rows x 1 head,
+// 128-byte swizzle; rows beyond `rows` read as zero.
+int make_map(CUtensorMap *map, const void *ptr, bool bf16, int d, int rows, int BH, int box_rows) {
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                          const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_common(const void *q, const void *k, const void *v, const void *o, const float *lse, int B, int H,
+                 int Nq, int Nk, int d, int causal, float scale, int dtype) {
+    if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0) return FA_ERR_INVALID_ARG;
+    if ((long long)B * H > INT32_MAX) return FA_ERR_INVALID_ARG;
+    if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16)) return FA_ERR_MISALIGNED;
+    if (lse != nullptr && !aligned(lse, 4)) return FA_ERR_MISALIGNED;
+    return FA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int auto_splits(int num_sms, long long rows, int Nk) {
+    // Enough CTAs for about eight waves at two resident CTAs per SM, at least one
+    // 64-key tile per split, at most 64 splits.
+    const long long target = 16LL * (num_sms > 0 ? num_sms : 148);
+    long long s = (target + rows - 1) / rows;
+    const long long tiles = (Nk + kDecBc - 1) / kDecBc;
+    if (s > tiles) s = tiles;
+    if (s > 64) s = 64;
+    if (s < 1) s = 1;
+    return (int)s;
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char *fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "ok";
+        case FA_ERR_INVALID_ARG: return "invalid argument";
+        case FA_ERR_UNSUPPORTED: return "unsupported head dimension (d must be 64 or 128)";
+        case FA_ERR_MISALIGNED: return "misaligned pointer (16-byte alignment required)";
+        case FA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case FA_ERR_CUDA: return "CUDA runtime error";
+        case FA_ERR_DEVICE_TIMEOUT: return "a device-side bounded wait ran out";
+        default: return "unknown status";
+    }
+}
+
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq, int Nk, int d,
+           int causal, float scale, fa_dtype dtype, fa_stream_t stream) {
+    int rc = check_common(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, dtype);
+    if (rc != FA_OK) return rc;
+    const int num_m = (Nq + kFwdBr - 1) / kFwdBr;
+    if (num_m > 65535) return FA_ERR_INVALID_ARG;
+    DeviceState *st = nullptr;
+    if ((rc = dev_state(&st)) != FA_OK) return rc;
+    const bool bf16 = dtype == FA_BF16;
+    const int BH = B * H;
+    CUtensorMap tq, tk, tv;
+    if (make_map(&tq, q, bf16, d, Nq, BH, kFwdBr) != FA_OK || make_map(&tk, k, bf16, d, Nk, BH, kFwdBc) != FA_OK ||
+        make_map(&tv, v, bf16, d, Nk, BH, kFwdBc) != FA_OK)
+        return FA_ERR_CUDA;
+    FwdArgs a;
+    a.o = o;
+    a.lse = lse;
+    a.status = st->status;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.num_m = num_m;
+    a.causal = causal;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    cudaError_t e = launch_fwd(d, bf16, tq, tk, tv, a, BH, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_splitkv_num_splits(int B, int H, int Nq, int Nk, int d) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return 0;
+    DeviceState *st = nullptr;
+    int sms = 148;
+    if (dev_state(&st) == FA_OK) sms = st->num_sms;
+    return auto_splits(sms, (long long)B * H * Nq, Nk);
+}
+
+int fa_splitkv_split_len(int Nk, int num_splits) {
+    if (Nk <= 0 || num_splits <= 0) return 0;
+    const int tiles = (Nk + kDecBc - 1) / kDecBc;
+    const int per = (tiles + num_splits - 1) / num_splits;
+    return per * kDecBc;
+}
+
+size_t fa_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return 0;
+    if (num_splits <= 0) num_splits = fa_splitkv_num_splits(B, H, Nq, Nk, d);
+    if (num_splits <= 0 || num_splits > kMaxSplits) return 0;
+    const size_t rows = (size_t)B * H * Nq;
+    return align256((size_t)num_splits * rows * d * sizeof(float)) + align256((size_t)num_splits * rows * sizeof(float));
+}
+
+int fa_splitkv_combine(const float *o_part, const float *lse_part, void *o, float *lse, int num_splits, int B, int H,
+                       int Nq, int d, fa_dtype dtype, fa_stream_t stream) {
+    if (o_part == nullptr || lse_part == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || Nq <= 0 || num_splits <= 0 || num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned(o_part, 16) || !aligned(o, 16) || !aligned(lse_part, 4)) return FA_ERR_MISALIGNED;
+    if (lse != nullptr && !aligned(lse, 4)) return FA_ERR_MISALIGNED;
+    const long long rows = (long long)B * H * Nq;
+    if ((rows + 3) / 4 > INT32_MAX) return FA_ERR_INVALID_ARG;
+    CombineArgs a;
+    a.o_part = o_part;
+    a.lse_part = lse_part;
+    a.o = o;
+    a.lse = lse;
+    a.num_splits = num_splits;
+    a.rows = rows;
+    cudaError_t e = launch_combine(d, dtype == FA_BF16, a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq, int Nk,
+                   int d, int causal, float scale, fa_dtype dtype, int num_splits, void *workspace,
+                   size_t workspace_bytes, fa_stream_t stream) {
+    int rc = check_common(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, dtype);
+    if (rc != FA_OK) return rc;
+    if (num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+    DeviceState *st = nullptr;
+    if ((rc = dev_state(&st)) != FA_OK) return rc;
+    const long long rows = (long long)B * H * Nq;
+    if (num_splits <= 0) num_splits = auto_splits(st->num_sms, rows, Nk);
+    if ((long long)num_splits * rows > INT32_MAX) return FA_ERR_INVALID_ARG;
+    const size_t need = fa_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits);
+    if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    const bool bf16 = dtype == FA_BF16;
+    const int BH = B * H;
+    CUtensorMap tk, tv;
+    if (make_map(&tk, k, bf16, d, Nk, BH, kDecBc) != FA_OK || make_map(&tv, v, bf16, d, Nk, BH, kDecBc) != FA_OK)
+        return FA_ERR_CUDA;
+    float *o_part = static_cast<float *>(workspace);
+    float *lse_part =
+        reinterpret_cast<float *>(static_cast<char *>(workspace) + align256((size_t)num_splits * rows * d * sizeof(float)));
+    SplitArgs a;
+    a.q = q;
+    a.o_part = o_part;
+    a.lse_part = lse_part;
+    a.status = st->status;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.BH = BH;
+    a.num_splits = num_splits;
+    a.split_len = fa_splitkv_split_len(Nk, num_splits);
+    a.causal = causal;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_splitkv(d, bf16, tk, tv, a, s);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    return fa_splitkv_combine(o_part, lse_part, o, lse, num_splits, B, H, Nq, d, dtype, stream);
+}
+
+int fa_get_device_status(fa_stream_t stream) {
+    DeviceState *st = nullptr;
+    int rc = dev_state(&st);
+    if (rc != FA_OK) return rc;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+        if (word & kDevErrTimeout) return FA_ERR_DEVICE_TIMEOUT;
+    }
+    if (cudaPeekAtLastError() != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// fa_internal.h -- host-side interface between the C ABI (fa_api.cu) and the
+// kernel translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+// Device-side error bits OR-ed into the per-device status word.
+constexpr int kDevErrTimeout = 1;
+
+// Tile shape of the fused forward kernel: 128 query rows per CTA (one TMEM
+// lane per row) and 128 keys per K/V tile.
+constexpr int kFwdBr = 128;
+constexpr int kFwdBc = 128;
+// Keys per tile of the split-KV kernel; split lengths are multiples of it.
+constexpr int kDecBc = 64;
+constexpr int kMaxSplits = 256;
+
+struct FwdArgs {
+    void *o;        // [BH, Nq, d] 16-bit
+    float *lse;     // [BH, Nq] or nullptr
+    int *status;    // device status word
+    int Nq, Nk;
+    int num_m;      // ceil(Nq / kFwdBr)
+    int causal;
+    float scale_log2;  // scale * log2(e)
+};
+
+struct SplitArgs {
+    const void *q;     // [BH, Nq, d] 16-bit
+    float *o_part;     // [S, BH, Nq, d] fp32
+    float *lse_part;   // [S, BH, Nq] fp32
+    int *status;
+    int Nq, Nk, BH;
+    int num_splits, split_len;
+    int causal;
+    float scale_log2;
+};
+
+struct CombineArgs {
+    const float *o_part;
+    const float *lse_part;
+    void *o;
+    float *lse;
+    int num_splits;
+    long long rows;  // BH * Nq
+};
+
+// Each launcher returns the CUDA error of the launch (cudaSuccess when queued).
+cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const FwdArgs &a, int BH, cudaStream_t stream);
+cudaError_t launch_splitkv(int d, bool bf16, const CUtensorMap &tk, const CUtensorMap &tv, const SplitArgs &a,
+                           cudaStream_t stream);
+cudaError_t launch_combine(int d, bool bf16, const CombineArgs &a, cudaStream_t stream);
+
+}  // namespace fa

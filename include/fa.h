@@ -1,0 +1,164 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact attention forward library (libfa.so).
+ *
+ * The operation (all entry points): for every batch b, head h and query row i,
+ *
+ *     O[b,h,i,:] = sum_j softmax_j( scale * q_i . k_j  + mask(i,j) ) * v_j
+ *     LSE[b,h,i] = ln sum_{j allowed} exp(scale * q_i . k_j)
+ *
+ * with mask(i,j) = -inf when causal and j > i + (Nk - Nq) (the diagonal is
+ * aligned to the bottom-right corner, which is the usual "row i sees j <= i"
+ * when Nq == Nk), else 0.  The computation follows the FlashAttention-2
+ * forward: Q row-blocks outer, K/V tiles inner, a running row max m and row
+ * sum l, the output rescaled by exp(m_old - m_new) and divided by l once at the
+ * end, and LSE = m + ln l written per row.  Sources: "6.2 FlashAttention V2
+ * explained" §3.2 (deferred rescaling), §5 (causal mask and block skipping),
+ * §6 (the forward algorithm with its L = m + log l output); "02 · FA2:
+ * parallelism and work partitioning" §2 (a grid over Q row-blocks, and for
+ * seqlen_q = 1 the split-KV partials (O, LSE) merged by a combine kernel).
+ *
+ * Layouts: q, o are [B, H, Nq, d]; k, v are [B, H, Nk, d]; all contiguous
+ * (row stride d elements), 16-bit (fp16 or bf16, the same for all four).
+ * lse is [B, H, Nq] fp32.  Accumulation is fp32.
+ *
+ * Ownership: the caller owns every buffer and the stream.  All pointers are
+ * device pointers unless stated otherwise.  The library allocates no device
+ * memory; it keeps only a per-device status word for device-side errors.
+ *
+ * Asynchrony: every launching call is asynchronous on `stream`.  Its return
+ * value reports host-side validation and launch errors only; errors raised on
+ * the device (a bounded wait that ran out) are reported by
+ * fa_get_device_status.
+ *
+ * Common validation (returned before anything is launched):
+ *   FA_ERR_INVALID_ARG   B, H, Nq, Nk <= 0; scale not finite or <= 0; a null
+ *                        q, k, v or o; an unknown dtype; causal not 0/1.
+ *   FA_ERR_UNSUPPORTED   d not 64 or 128.
+ *   FA_ERR_MISALIGNED    q, k, v, o not 16-byte aligned (TMA requirement),
+ *                        lse not 4-byte aligned.
+ *   FA_ERR_CUDA          a CUDA runtime error at launch.
+ * Inputs q, k, v are never written; o and lse are fully overwritten.  A row
+ * that sees no key (only possible when causal and Nq > Nk) gets O = 0 and
+ * LSE = -inf.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *fa_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum { FA_F16 = 0, FA_BF16 = 1 } fa_dtype;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = -1,
+    FA_ERR_UNSUPPORTED = -2,
+    FA_ERR_MISALIGNED = -3,
+    FA_ERR_WORKSPACE = -4,
+    FA_ERR_CUDA = -5,
+    FA_ERR_DEVICE_TIMEOUT = -6
+} fa_status;
+
+/*
+ * Fused attention forward (one launch): one CTA per 128-row Q tile and head,
+ * K/V tiles streamed by TMA, both GEMMs on tcgen05 tensor cores with fp32
+ * accumulators in tensor memory, online softmax with deferred 1/l.  Under
+ * causal masking, K/V tiles entirely above the diagonal are skipped and only
+ * tiles that straddle it (or the ragged Nk tail) are masked element-wise.
+ * ("6.2 FlashAttention V2 explained" §6; "02 · FA2" §2 and §4.)
+ *
+ *   q, k, v  inputs, layouts above.
+ *   o        output [B, H, Nq, d], same dtype as the inputs.
+ *   lse      output [B, H, Nq] fp32 (natural log of the scaled scores), or NULL.
+ *   scale    score scale, normally 1/sqrt(d).
+ * Returns FA_OK or one of the validation errors above.
+ */
+FA_API int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+           int B, int H, int Nq, int Nk, int d, int causal, float scale,
+           fa_dtype dtype, fa_stream_t stream);
+
+/*
+ * Workspace bytes that fa_fwd_splitkv needs for `num_splits` splits:
+ * fp32 partial outputs [num_splits, B, H, Nq, d] followed by fp32 partial LSEs
+ * [num_splits, B, H, Nq], each region 256-byte aligned.  num_splits <= 0 means
+ * the value fa_splitkv_num_splits would choose.  Returns 0 on invalid sizes.
+ */
+FA_API size_t fa_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
+
+/*
+ * The number of splits fa_fwd_splitkv uses when passed num_splits <= 0
+ * (enough CTAs to fill the GPU several times over, at most 64), and the key
+ * count of every split but the last: split s covers keys
+ * [s * split_len, min((s + 1) * split_len, Nk)), where split_len is a multiple
+ * of the 64-key tile.  A split may be empty when num_splits exceeds the tile count.
+ */
+FA_API int fa_splitkv_num_splits(int B, int H, int Nq, int Nk, int d);
+FA_API int fa_splitkv_split_len(int Nk, int num_splits);
+
+/*
+ * Split-KV attention forward (flash-decoding), written for Nq = 1 but valid for
+ * any Nq: the keys of each (b, h) are cut into num_splits contiguous ranges;
+ * one CTA per (split, query row, head) computes the range's normalised partial
+ * output O_s and LSE_s on CUDA cores (fp32), then a combine kernel merges them
+ * ("02 · FA2: parallelism and work partitioning" §2, decode / split-KV).
+ * Two launches on `stream`; the partials live in the caller's workspace.
+ *
+ *   num_splits       1..256, or <= 0 for fa_splitkv_num_splits.
+ *   workspace        device buffer of at least
+ *                    fa_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits)
+ *                    bytes, 256-byte aligned; its contents are overwritten.
+ * Errors: the common ones, plus FA_ERR_WORKSPACE when the workspace is NULL,
+ * misaligned or too small, and FA_ERR_INVALID_ARG when num_splits > 256.
+ */
+FA_API int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                   int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                   fa_dtype dtype, int num_splits, void *workspace, size_t workspace_bytes,
+                   fa_stream_t stream);
+
+/*
+ * LSE-weighted merge of split partials, per row r of B*H*Nq rows:
+ *   M = max_s LSE_s;  w_s = exp(LSE_s - M);
+ *   O = sum_s w_s O_s / sum_s w_s;  LSE = M + ln sum_s w_s.
+ * A row whose partials are all empty (every LSE_s = -inf) gets O = 0, LSE = -inf.
+ *
+ *   o_part    fp32 [num_splits, B, H, Nq, d], normalised partial outputs.
+ *   lse_part  fp32 [num_splits, B, H, Nq].
+ *   o         [B, H, Nq, d] in `dtype`;  lse  [B, H, Nq] fp32 or NULL.
+ * Errors: FA_ERR_INVALID_ARG (sizes, null pointers, num_splits not in 1..256),
+ * FA_ERR_UNSUPPORTED (d), FA_ERR_MISALIGNED (o_part, o not 16-byte aligned).
+ */
+FA_API int fa_splitkv_combine(const float *o_part, const float *lse_part, void *o, float *lse,
+                       int num_splits, int B, int H, int Nq, int d, fa_dtype dtype,
+                       fa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns FA_ERR_DEVICE_TIMEOUT if any kernel of
+ * this library on the current device gave up a bounded wait since the last
+ * call (the flag is cleared), FA_ERR_CUDA if the context reports an error,
+ * else FA_OK.
+ */
+FA_API int fa_get_device_status(fa_stream_t stream);
+
+/* Static description of a status code. Never NULL. */
+FA_API const char *fa_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+FA_API int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

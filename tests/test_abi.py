@@ -1,0 +1,86 @@
+"""libfa.so builds, loads and exports every symbol include/fa.h declares; host-side checks (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_forward_03_gb300 import build
+    import exact_attention_forward_03_gb300 as fa
+
+    build.build()
+    return fa.load_library()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    return sorted(set(re.findall(r"FA_API\s+[\w\s\*]+?\b(fa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_symbols()
+    assert {"fa_fwd", "fa_fwd_splitkv", "fa_splitkv_combine", "fa_get_device_status"} <= set(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import exact_attention_forward_03_gb300 as fa
+
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in fa.EXPORTS
+
+
+def test_version_and_status_strings(lib):
+    assert lib.fa_version() >= 100
+    for code in range(-6, 1):
+        assert lib.fa_status_string(code)
+    assert lib.fa_status_string(12345) == b"unknown status"
+
+
+def test_validation_without_gpu(lib):
+    """Argument checks run before any CUDA call, so they work on a host without a GPU."""
+    p = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: the call is rejected first
+    f = lib.fa_fwd
+    assert f(None, p, p, p, None, 1, 1, 8, 8, 64, 0, 0.125, 0, None) == -1       # null q
+    assert f(p, p, p, p, None, 0, 1, 8, 8, 64, 0, 0.125, 0, None) == -1          # B = 0
+    assert f(p, p, p, p, None, 1, 1, 8, 8, 96, 0, 0.125, 0, None) == -2          # d = 96
+    assert f(p, p, p, p, None, 1, 1, 8, 8, 64, 0, -1.0, 0, None) == -1           # scale <= 0
+    assert f(p, p, p, p, None, 1, 1, 8, 8, 64, 0, float("nan"), 0, None) == -1  # scale NaN
+    assert f(p, p, p, p, None, 1, 1, 8, 8, 64, 2, 0.125, 0, None) == -1          # causal = 2
+    assert f(p, p, p, p, None, 1, 1, 8, 8, 64, 0, 0.125, 7, None) == -1          # dtype
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    assert f(odd, p, p, p, None, 1, 1, 8, 8, 64, 0, 0.125, 0, None) == -3        # q not 16-byte aligned
+    assert f(p, p, p, p, ctypes.c_void_p((1 << 20) + 2), 1, 1, 8, 8, 64, 0, 0.125, 0, None) == -3
+    c = lib.fa_splitkv_combine
+    assert c(None, p, p, None, 4, 1, 1, 1, 64, 0, None) == -1
+    assert c(p, p, p, None, 0, 1, 1, 1, 64, 0, None) == -1
+    assert c(p, p, p, None, 300, 1, 1, 1, 64, 0, None) == -1
+    assert c(p, p, p, None, 4, 1, 1, 1, 32, 0, None) == -2
+
+
+def test_split_planning(lib):
+    assert lib.fa_splitkv_split_len(16384, 16) == 1024
+    assert lib.fa_splitkv_split_len(1000, 8) == 128
+    assert lib.fa_splitkv_split_len(65, 32) == 64
+    for Nk, S in [(1, 1), (65, 32), (16384, 8), (999, 7)]:
+        L = lib.fa_splitkv_split_len(Nk, S)
+        assert L % 64 == 0 and L * S >= Nk and L * (S - 1) < Nk + 64 * S
+    rows, d, S = 1024, 128, 16
+    ws = lib.fa_splitkv_workspace_bytes(32, 32, 1, 16384, d, S)
+    assert ws >= S * rows * (d + 1) * 4 and ws % 256 == 0
+    assert lib.fa_splitkv_workspace_bytes(32, 32, 1, 16384, 96, S) == 0
+    assert lib.fa_splitkv_workspace_bytes(32, 32, 1, 16384, d, 300) == 0
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    import exact_attention_forward_03_gb300 as fa
+
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        fa.fwd(q, q, q)

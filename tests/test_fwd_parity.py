@@ -1,0 +1,176 @@
+"""fa_fwd (tcgen05 fused forward) against the fp64 oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attn_inputs
+import oracle
+from parity import compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import exact_attention_forward_03_gb300 as fa
+    from exact_attention_forward_03_gb300 import build
+
+    build.build()
+    fa.load_library()
+    oracle.set_threads(16)
+    return fa
+
+
+def run_case(fa, B, H, Nq, Nk, d, dtype, causal, seed, scale=None):
+    q, k, v = attn_inputs.make_qkv(B, H, Nq, Nk, d, dtype, seed, "cuda")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o, lse = fa.fwd(q, k, v, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.get_device_status() == fa.FA_OK
+    o_ref, lse_ref = oracle.attention(q, k, v, causal, scale)
+    return compare(o, o_ref, lse, lse_ref, q.dtype, f"B{B} H{H} Nq{Nq} Nk{Nk} d{d} {dtype} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_d64_f16(fa, causal):
+    w = attn_inputs.WORKLOADS["tiny_d64_f16_causal" if causal else "tiny_d64_f16"]
+    run_case(fa, w.B, w.H, w.Nq, w.Nk, w.d, w.dtype, causal, w.seed)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_b4h16_n1024_d64_f16_all_rows(fa, causal):
+    w = attn_inputs.WORKLOADS["b4h16_n1024_d64_f16"]
+    run_case(fa, w.B, w.H, w.Nq, w.Nk, w.d, w.dtype, causal, w.seed)
+
+
+RAGGED = [
+    # B, H, Nq, Nk, d, dtype, causal
+    (1, 2, 1, 1, 64, "f16", False),
+    (1, 2, 17, 17, 128, "bf16", True),
+    (2, 1, 127, 129, 64, "bf16", False),
+    (1, 3, 129, 127, 128, "f16", False),
+    (1, 2, 255, 255, 128, "bf16", True),
+    (1, 1, 300, 300, 64, "f16", True),
+    (2, 2, 384, 384, 128, "bf16", True),
+    (1, 2, 200, 520, 128, "bf16", True),   # Nq < Nk: bottom-right diagonal
+    (1, 2, 520, 200, 64, "f16", True),     # Nq > Nk: first 320 rows see no key
+    (1, 1, 1, 700, 128, "bf16", False),    # one query row, many tiles
+    (1, 1, 640, 1, 64, "bf16", False),     # one key
+    (2, 3, 700, 333, 128, "f16", False),
+]
+
+
+@pytest.mark.parametrize("case", RAGGED, ids=lambda c: "B{}H{}_q{}_k{}_d{}_{}_{}".format(*c[:6], "c" if c[6] else "nc"))
+def test_ragged_shapes(fa, case):
+    B, H, Nq, Nk, d, dtype, causal = case
+    run_case(fa, B, H, Nq, Nk, d, dtype, causal, seed=7 * Nq + Nk)
+
+
+def _sampled(fa, wname, count=1024):
+    w = attn_inputs.WORKLOADS[wname]
+    q, k, v = attn_inputs.make_workload(w, "cuda")
+    o, lse = fa.fwd(q, k, v, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.get_device_status() == fa.FA_OK
+    pairs = attn_inputs.sample_rows(w.Nq, w.B * w.H, count, seed=w.seed)
+    o_ref, lse_ref = oracle.sampled_rows(q, k, v, pairs, w.causal, w.scale)
+    of = o.view(-1, w.Nq, w.d)
+    lf = lse.view(-1, w.Nq)
+    idx_bh = torch.tensor([p[0] for p in pairs], device=o.device)
+    idx_r = torch.tensor([p[1] for p in pairs], device=o.device)
+    stats = compare(of[idx_bh, idx_r], o_ref, lf[idx_bh, idx_r], lse_ref, q.dtype, wname)
+    assert torch.isfinite(o).all()
+    return stats
+
+
+def test_b2h32_n8192_d128_bf16_causal_sampled(fa):
+    _sampled(fa, "b2h32_n8192_d128_bf16_causal")
+
+
+def test_b2h32_n8192_d128_bf16_noncausal_sampled(fa):
+    _sampled(fa, "b2h32_n8192_d128_bf16")
+
+
+def test_b1h32_n32768_d128_bf16_causal_sampled(fa):
+    _sampled(fa, "b1h32_n32768_d128_bf16_causal", count=512)
+
+
+def test_constant_v_gives_constant_o(fa):
+    q, k, _ = attn_inputs.make_qkv(1, 2, 300, 300, 128, "bf16", 31, "cuda")
+    v = torch.full_like(k, 0.8125)
+    for causal in (False, True):
+        o, _ = fa.fwd(q, k, v, causal=causal)
+        compare(o, np.full(o.shape, 0.8125), None, None, q.dtype, f"constant V causal={causal}")
+
+
+def test_causal_row0_is_v0(fa):
+    for d, dt in ((64, "f16"), (128, "bf16")):
+        q, k, v = attn_inputs.make_qkv(2, 2, 256, 256, d, dt, 32, "cuda")
+        o, lse = fa.fwd(q, k, v, causal=True)
+        assert torch.equal(o[:, :, 0], v[:, :, 0])
+        s00 = (q[:, :, 0].double() * k[:, :, 0].double()).sum(-1) / math.sqrt(d)
+        assert torch.allclose(lse[:, :, 0].double(), s00, atol=1e-4, rtol=0)
+
+
+def test_causal_never_reads_future_tiles(fa):
+    """NaN in V rows 128..255 must not reach rows 0..127 (their K/V tile range ends at 128)."""
+    q, k, v = attn_inputs.make_qkv(1, 2, 256, 256, 128, "bf16", 33, "cuda")
+    v2 = v.clone()
+    v2[:, :, 128:] = float("nan")
+    k2 = k.clone()
+    k2[:, :, 128:] = float("nan")
+    o, lse = fa.fwd(q, k2, v2, causal=True)
+    o_ref, lse_ref = oracle.attention(q[:, :, :128], k[:, :, :128], v[:, :, :128], True, 1 / math.sqrt(128))
+    compare(o[:, :, :128], o_ref, lse[:, :, :128], lse_ref, q.dtype, "future tiles")
+
+
+def test_growing_row_max_needs_l_rescale(fa):
+    """Keys whose scores rise with j: the running max moves in every tile (l * alpha matters)."""
+    Nk, d = 1024, 128
+    q = torch.ones(1, 1, 256, d, device="cuda", dtype=torch.bfloat16) * 0.25
+    ramp = torch.linspace(-2.0, 2.0, Nk, device="cuda")[:, None].expand(Nk, d)
+    k = ramp[None, None].to(torch.bfloat16).contiguous()
+    v = torch.randn(1, 1, Nk, d, device="cuda", generator=torch.Generator("cuda").manual_seed(5)).to(torch.bfloat16)
+    for causal in (False, True):
+        o, lse = fa.fwd(q, k, v, causal=causal, scale=0.125)
+        o_ref, lse_ref = oracle.attention(q, k, v, causal, 0.125)
+        compare(o, o_ref, lse, lse_ref, q.dtype, f"growing max causal={causal}")
+
+
+def test_large_scores_stay_finite(fa):
+    """Scores of size ~1e3 (scale 1, large q and k) must not overflow."""
+    q, k, v = attn_inputs.make_qkv(1, 2, 200, 300, 64, "bf16", 34, "cuda")
+    q = (q * 8).contiguous()
+    k = (k * 8).contiguous()
+    for causal in (False, True):
+        o, lse = fa.fwd(q, k, v, causal=causal, scale=1.0)
+        assert torch.isfinite(o).all()
+        o_ref, lse_ref = oracle.attention(q, k, v, causal, 1.0)
+        compare(o, o_ref, lse, lse_ref, q.dtype, f"large scores causal={causal}")
+
+
+def test_lse_optional(fa):
+    q, k, v = attn_inputs.make_qkv(1, 1, 130, 130, 64, "f16", 35, "cuda")
+    o1, _ = fa.fwd(q, k, v, causal=True, want_lse=False)
+    o2, _ = fa.fwd(q, k, v, causal=True)
+    assert torch.equal(o1, o2)
+
+
+def test_deterministic(fa):
+    q, k, v = attn_inputs.make_qkv(2, 4, 1000, 1000, 128, "bf16", 36, "cuda")
+    a = fa.fwd(q, k, v, causal=True)
+    b = fa.fwd(q, k, v, causal=True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_nonzero_stream(fa):
+    q, k, v = attn_inputs.make_qkv(1, 4, 512, 512, 128, "bf16", 37, "cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o, lse = fa.fwd(q, k, v, causal=False)
+    s.synchronize()
+    o2, lse2 = fa.fwd(q, k, v, causal=False)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
