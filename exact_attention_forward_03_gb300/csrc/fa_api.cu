@@ -128,8 +128,8 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
            int causal, float scale, fa_dtype dtype, fa_stream_t stream) {
     int rc = check_common(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, dtype);
     if (rc != FA_OK) return rc;
-    const int num_m = (Nq + kFwdBr - 1) / kFwdBr;
-    if (num_m > 65535) return FA_ERR_INVALID_ARG;
+    const int num_m = (Nq + kFwdTilesPerCta * kFwdBr - 1) / (kFwdTilesPerCta * kFwdBr);
+    if (B * H > 65535) return FA_ERR_INVALID_ARG;  // grid.y limit
     DeviceState *st = nullptr;
     if ((rc = dev_state(&st)) != FA_OK) return rc;
     const bool bf16 = dtype == FA_BF16;

@@ -1,32 +1,46 @@
 // fa_fwd_sm103.cu -- fused exact attention forward on sm_103a tensor cores.
 //
-// One CTA computes one 128-row Q tile of one (batch, head):
+// One CTA computes two 128-row Q tiles (A and B, 256 consecutive query rows) of
+// one (batch, head):
 //   O_i = sum_j softmax_j(scale * q_i . k_j + mask) v_j,  LSE_i = m_i + ln l_i
 // following the FlashAttention-2 forward ("6.2 FlashAttention V2 explained",
-// §6): the Q tile stays on chip, K/V tiles stream past it, a running row max m
-// and row sum l are kept per row, the accumulator is rescaled by
+// §6): the Q tiles stay on chip, K/V tiles stream past them, a running row max
+// m and row sum l are kept per row, the accumulator is rescaled by
 // exp(m_old - m_new) and divided by l once at the end (§3.2; "02 · FA2", §1).
-// Causal masking visits only K/V tiles up to the diagonal and masks element-wise
-// only on tiles that straddle it or the ragged Nk tail (§5.3; "02 · FA2", §4).
+// Causal masking visits only K/V tiles up to the diagonal and masks
+// element-wise only on tiles that straddle it or the ragged Nk tail (§5.3;
+// "02 · FA2", §4).
 //
-// Roles (warp specialisation, 6 warps):
-//   warp 0     TMA producer: Q once, then K_0, V_0, K_1, V_1, ... through a
-//              ring of shared-memory slots guarded by full/empty mbarriers.
-//   warp 1     owns tensor memory; one lane issues tcgen05.mma:
-//              S_j = Q K_j^T into one of two TMEM S buffers (fp32), and
-//              O += P_j V_j with P read from TMEM (the A operand) and V from
-//              shared memory (MN-major B operand).
-//   warps 2-5  softmax, one thread per query row (TMEM lane = row): load the
-//              S row, mask, update (m, l) in base 2, write P as 16-bit into
-//              TMEM, rescale the O row by alpha when the max moved, and in the
-//              epilogue normalise by 1/l and write O and LSE.
-// The MMA of S_{j+1} runs while the softmax of tile j runs (two S buffers).
+// Roles (warp specialisation, 3 warpgroups):
+//   warps 0-3  softmax of Q tile A, one thread per query row (TMEM lane = row)
+//   warps 4-7  softmax of Q tile B
+//   warp 8     TMA producer: both Q tiles once, then K_0, V_0, K_1, V_1, ...
+//              through a ring of shared-memory slots (full/empty mbarriers)
+//   warp 9     owns tensor memory; one lane issues every tcgen05.mma
+//   warps 10-11 idle (they complete the third warpgroup)
+// Each SM sub-partition holds one warp of each warpgroup.  The launch gives
+// every thread 168 registers; the third warpgroup drops to 88 and the two
+// softmax warpgroups rise to 208 (88 + 2 * 208 = 3 * 168), enough to hold a
+// whole 128-column S row.
+// The two Q tiles ping-pong on the tensor core: while the softmax warps of one
+// tile work on S_j, the tensor core runs O += P_j V_j and S_{j+1} = Q K_{j+1}^T
+// of the other tile, so exp2 and the rescale stay off the tensor pipe's path.
+// MMA issue order per K/V step j:  PV_A(j), S_A(j+1), PV_B(j), S_B(j+1).
 //
-// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O [256,256+d),
-// P [384,448) and, on masked tiles, P_lo [448,512).  On a masked tile P is
-// written as a 16-bit head plus a 16-bit remainder (P = P_hi + P_lo) and both
-// are multiplied into O: rows with few visible keys are then not limited by
-// the 16-bit rounding of their few large weights.
+// Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+d),
+// O_B [256+d,256+2d).  P_X overwrites the first 64 columns of S_X as 16-bit
+// pairs once the softmax thread holds its S row in registers; on tiles that
+// need a mask the 16-bit remainder P - P_hi goes to the next 64 columns and is
+// multiplied into O as well (rows near the diagonal see few keys, so one
+// 16-bit rounding of their few large weights would dominate their error).
+// tcgen05.mma operations of one thread run in issue order, so S_X(j+1) writes
+// S_X only after PV_X(j) has read P_X(j); and the commit that signals S_X(j+1)
+// also covers PV_X(j), so the softmax may rescale O_X as soon as S_X(j+1) is ready.
+//
+// The rescale of O by alpha = 2^(m_old - m_new) is done only when the row max
+// of some row in the warp grew by more than 2^8: otherwise m stays and p may
+// reach 2^8, which changes nothing in exact arithmetic (O and l share the same
+// stale max) and keeps fp16/bf16/fp32 far from overflow.
 //
 // Every mbarrier wait is bounded (%globaltimer); on expiry the CTA records
 // the timeout in the status word, stops issuing work, waits (bounded) for its
@@ -36,29 +50,32 @@
 
 namespace fa {
 
-constexpr int kFwdThreads = 192;
+constexpr int kFwdThreads = 384;
+constexpr uint32_t kRegsSoftmax = 208;
+constexpr uint32_t kRegsOther = 88;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct FwdCfg {
     static_assert(D == 64 || D == 128, "head dim");
-    static constexpr int kStages = (D == 128) ? 4 : 6;
+    static constexpr int kStages = (D == 128) ? 5 : 8;
     static constexpr int kBlocks = D / 64;               // 128-byte swizzle blocks per row
-    static constexpr int kQBlockBytes = kFwdBr * 128;    // one 64-column block of the Q tile
+    static constexpr int kQBlockBytes = kFwdBr * 128;    // one 64-column block of a Q tile
     static constexpr int kKVBlockBytes = kFwdBc * 128;   // one 64-column block of a K/V tile
-    static constexpr int kQBytes = kFwdBr * D * 2;
-    static constexpr int kTileBytes = kFwdBc * D * 2;
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffRing = kQBytes;
+    static constexpr int kQBytes = kFwdBr * D * 2;       // one Q tile
+    static constexpr int kTileBytes = kFwdBc * D * 2;    // one K or V tile
+    static constexpr int kOffQ = 0;                      // Q_A, then Q_B
+    static constexpr int kOffRing = kFwdTilesPerCta * kQBytes;
     static constexpr int kOffBar = kOffRing + kStages * kTileBytes;
-    // barriers: q_full, full[S], empty[S], s_full[2], p_full[2], o_done, mma_fin
-    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1;
+    // barriers: q_full, full[S], empty[S], s_full[2], p_full[2], o_final[2], mma_fin
+    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    // Unused tail after the last slot: keeps any tensor-core operand read that a
-    // descriptor could reach from the last slot inside this CTA's allocation.
-    static constexpr int kGuardBytes = 32768;
-    static constexpr int kSmemBytes = kOffMisc + 16 + kGuardBytes + 1024;  // + slack to align the base
-    static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256, kTmemP = 384, kTmemPlo = 448;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+    static constexpr uint32_t kTmemPlo = 64;  // offset of P_lo inside S_X
     static constexpr uint32_t kTmemCols = 512;
+    __device__ static constexpr uint32_t tmem_s(int x) { return x == 0 ? 0u : 128u; }
+    __device__ static constexpr uint32_t tmem_o(int x) { return x == 0 ? 256u : 256u + D; }
 };
 
 // Tile j needs element masks when it crosses the ragged end of K or, under
@@ -66,6 +83,14 @@ struct FwdCfg {
 __device__ __forceinline__ bool fwd_tile_needs_mask(int j, int q0, int Nq, int Nk, int causal) {
     const int last_key = (j + 1) * kFwdBc - 1;
     return (last_key >= Nk) || (causal && last_key > q0 + (Nk - Nq));
+}
+
+// K/V tiles that Q rows [q0, q0+128) must visit (0 when the tile holds no row).
+__device__ __forceinline__ int fwd_tile_count(int q0, int Nq, int Nk, int causal) {
+    if (q0 >= Nq) return 0;
+    int kv_end = Nk;
+    if (causal) kv_end = min(Nk, min(q0 + kFwdBr, Nq) + (Nk - Nq));
+    return kv_end > 0 ? (kv_end + kFwdBc - 1) / kFwdBc : 0;
 }
 
 template <int D, bool BF16>
@@ -82,23 +107,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int m_block = args.num_m - 1 - (int)blockIdx.y;  // heaviest causal tiles first
-    const int q0 = m_block * kFwdBr;
+    // Consecutive CTAs take consecutive row blocks of one head, heaviest causal
+    // block first, so the CTAs resident at any time share a few heads' K/V in L2.
+    const int bh = blockIdx.y;
+    const int q0 = (args.num_m - 1 - (int)blockIdx.x) * (kFwdTilesPerCta * kFwdBr);
     const int Nq = args.Nq, Nk = args.Nk, causal = args.causal;
-
-    int kv_end = Nk;
-    if (causal) kv_end = min(Nk, min(q0 + kFwdBr, Nq) + (Nk - Nq));
-    const int n_tiles = kv_end > 0 ? (kv_end + kFwdBc - 1) / kFwdBc : 0;
+    const int nA = fwd_tile_count(q0, Nq, Nk, causal);
+    const int nB = fwd_tile_count(q0 + kFwdBr, Nq, Nk, causal);
+    const int n_max = max(nA, nB);
 
     auto bar = [&](int idx) -> uint32_t { return sb + C::kOffBar + 8u * (uint32_t)idx; };
-    const int B_QFULL = 0;
+    constexpr int B_QFULL = 0;
     auto B_FULL = [](int s) { return 1 + s; };
     auto B_EMPTY = [](int s) { return 1 + C::kStages + s; };
-    auto B_SFULL = [](int b) { return 1 + 2 * C::kStages + b; };
-    auto B_PFULL = [](int b) { return 3 + 2 * C::kStages + b; };
-    const int B_ODONE = 5 + 2 * C::kStages;
-    const int B_MMAFIN = 6 + 2 * C::kStages;
+    auto B_SFULL = [](int x) { return 1 + 2 * C::kStages + x; };
+    auto B_PFULL = [](int x) { return 3 + 2 * C::kStages + x; };
+    auto B_OFINAL = [](int x) { return 5 + 2 * C::kStages + x; };
+    constexpr int B_MMAFIN = 7 + 2 * C::kStages;
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
     int *status = args.status;
@@ -109,11 +134,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_init(bar(B_FULL(s)), 1);
             mbar_init(bar(B_EMPTY(s)), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(B_SFULL(b)), 1);
-            mbar_init(bar(B_PFULL(b)), 128);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bar(B_SFULL(x)), 1);
+            mbar_init(bar(B_PFULL(x)), 128);
+            mbar_init(bar(B_OFINAL(x)), 1);
         }
-        mbar_init(bar(B_ODONE), 1);
         mbar_init(bar(B_MMAFIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -122,7 +147,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
     }
-    if (warp == 1) {
+    if (warp == 9) {
         tmem_alloc(sb + C::kOffMisc, C::kTmemCols);
         tmem_relinquish();
     }
@@ -131,14 +156,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 0) {
+    if (warp >= 8) regs_decrease<kRegsOther>();
+    if (warp == 8) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0 && n_tiles > 0) {
+        if (lane == 0 && n_max > 0) {
             uint32_t pend_mask = 0, pend_par = 0;
-            mbar_arrive_expect_tx(bar(B_QFULL), C::kQBytes);
-            for (int b = 0; b < C::kBlocks; ++b)
-                tma_load_3d(sb + C::kOffQ + b * C::kQBlockBytes, &tmQ, b * 64, q0, bh, bar(B_QFULL));
-            for (int t = 0; t < 2 * n_tiles; ++t) {
+            mbar_arrive_expect_tx(bar(B_QFULL), kFwdTilesPerCta * C::kQBytes);
+            for (int x = 0; x < kFwdTilesPerCta; ++x)
+                for (int b = 0; b < C::kBlocks; ++b)
+                    tma_load_3d(sb + C::kOffQ + x * C::kQBytes + b * C::kQBlockBytes, &tmQ, b * 64,
+                                q0 + x * kFwdBr, bh, bar(B_QFULL));
+            for (int t = 0; t < 2 * n_max; ++t) {
                 const int s = t % C::kStages;
                 const uint32_t it = (uint32_t)(t / C::kStages);
                 if (!mbar_wait_bounded(bar(B_EMPTY(s)), (it & 1u) ^ 1u, abort_flag, status)) break;
@@ -157,91 +185,102 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int s = 0; s < C::kStages; ++s)
                 if (pend_mask & (1u << s)) mbar_wait_bounded(bar(B_FULL(s)), (pend_par >> s) & 1u, &no_abort, status);
         }
-    } else if (warp == 1) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n_tiles > 0) {
+        if (lane == 0 && n_max > 0) {
             constexpr uint32_t idesc_qk = idesc_f16(128, kFwdBc, BF16, false);
             constexpr uint32_t idesc_pv = idesc_f16(128, D, BF16, true);
-            const uint32_t qa = sb + C::kOffQ;
-            bool ok = mbar_wait_bounded(bar(B_QFULL), 0, abort_flag, status);
-            for (int j = 0; ok && j <= n_tiles; ++j) {
-                if (j < n_tiles) {
-                    // S_j = Q K_j^T  (K-major A and B, 16 keys of d per instruction)
-                    const int t = 2 * j;
-                    const int s = t % C::kStages;
-                    if (!mbar_wait_bounded(bar(B_FULL(s)), (uint32_t)(t / C::kStages) & 1u, abort_flag, status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t ka = sb + C::kOffRing + s * C::kTileBytes;
-                    const uint32_t dS = tmem + ((j & 1) ? C::kTmemS1 : C::kTmemS0);
+            const int n_x[2] = {nA, nB};
+            auto slot_of = [](int t) { return t % C::kStages; };
+            auto par_of = [](int t) { return (uint32_t)(t / C::kStages) & 1u; };
+            // S_X(j) = Q_X K_j^T: K-major A and B, 16 of the d columns per instruction.
+            auto issue_s = [&](int x, int j) {
+                const uint32_t qa = sb + C::kOffQ + x * C::kQBytes;
+                const uint32_t ka = sb + C::kOffRing + slot_of(2 * j) * C::kTileBytes;
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t off_q = (k >> 2) * C::kQBlockBytes + (k & 3) * 32;
-                        const uint32_t off_k = (k >> 2) * C::kKVBlockBytes + (k & 3) * 32;
-                        umma_ss(dS, sdesc_sw128(qa + off_q, 16, 1024), sdesc_sw128(ka + off_k, 16, 1024), idesc_qk,
-                                k > 0 ? 1u : 0u);
-                    }
-                    umma_commit(bar(B_SFULL(j & 1)));
-                    umma_commit(bar(B_EMPTY(s)));
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off_q = (k >> 2) * C::kQBlockBytes + (k & 3) * 32;
+                    const uint32_t off_k = (k >> 2) * C::kKVBlockBytes + (k & 3) * 32;
+                    umma_ss(tmem + C::tmem_s(x), sdesc_sw128(qa + off_q, 16, 1024),
+                            sdesc_sw128(ka + off_k, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
                 }
-                if (j > 0) {
-                    // O += P_{j-1} V_{j-1}  (P from TMEM, V MN-major from shared memory)
-                    const int jj = j - 1;
-                    const int t = 2 * jj + 1;
-                    const int s = t % C::kStages;
-                    if (!mbar_wait_bounded(bar(B_PFULL(jj & 1)), (uint32_t)(jj >> 1) & 1u, abort_flag, status) ||
-                        !mbar_wait_bounded(bar(B_FULL(s)), (uint32_t)(t / C::kStages) & 1u, abort_flag, status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t va = sb + C::kOffRing + s * C::kTileBytes;
+                umma_commit(bar(B_SFULL(x)));
+            };
+            // O_X += P_X(j) V_j: P from TMEM, V as an MN-major operand, 16 keys per instruction.
+            auto issue_pv = [&](int x, int j) {
+                const uint32_t va = sb + C::kOffRing + slot_of(2 * j + 1) * C::kTileBytes;
+#pragma unroll
+                for (int k = 0; k < kFwdBc / 16; ++k)
+                    umma_ts(tmem + C::tmem_o(x), tmem + C::tmem_s(x) + 8 * k,
+                            sdesc_sw128(va + k * 2048, C::kKVBlockBytes, 1024), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+                if (fwd_tile_needs_mask(j, q0 + x * kFwdBr, Nq, Nk, causal)) {
 #pragma unroll
                     for (int k = 0; k < kFwdBc / 16; ++k)
-                        umma_ts(tmem + C::kTmemO, tmem + C::kTmemP + 8 * k,
-                                sdesc_sw128(va + k * 2048, C::kKVBlockBytes, 1024), idesc_pv,
-                                (jj > 0 || k > 0) ? 1u : 0u);
-                    if (fwd_tile_needs_mask(jj, q0, Nq, Nk, causal)) {
-#pragma unroll
-                        for (int k = 0; k < kFwdBc / 16; ++k)
-                            umma_ts(tmem + C::kTmemO, tmem + C::kTmemPlo + 8 * k,
-                                    sdesc_sw128(va + k * 2048, C::kKVBlockBytes, 1024), idesc_pv, 1u);
-                    }
-                    umma_commit(bar(B_ODONE));
-                    umma_commit(bar(B_EMPTY(s)));
+                        umma_ts(tmem + C::tmem_o(x), tmem + C::tmem_s(x) + C::kTmemPlo + 8 * k,
+                                sdesc_sw128(va + k * 2048, C::kKVBlockBytes, 1024), idesc_pv, 1u);
                 }
+                if (j == n_x[x] - 1) umma_commit(bar(B_OFINAL(x)));
+            };
+            bool ok = mbar_wait_bounded(bar(B_QFULL), 0, abort_flag, status) &&
+                      mbar_wait_bounded(bar(B_FULL(slot_of(0))), par_of(0), abort_flag, status);
+            if (ok) {
+                tc_fence_after();
+                if (nA > 0) issue_s(0, 0);
+                if (nB > 0) issue_s(1, 0);
+                umma_commit(bar(B_EMPTY(slot_of(0))));
+            }
+            for (int j = 0; ok && j < n_max; ++j) {
+                const bool next = j + 1 < n_max;
+                ok = mbar_wait_bounded(bar(B_FULL(slot_of(2 * j + 1))), par_of(2 * j + 1), abort_flag, status) &&
+                     (!next || mbar_wait_bounded(bar(B_FULL(slot_of(2 * j + 2))), par_of(2 * j + 2), abort_flag, status));
+                for (int x = 0; ok && x < 2; ++x) {
+                    if (j < n_x[x]) {
+                        if (!mbar_wait_bounded(bar(B_PFULL(x)), (uint32_t)j & 1u, abort_flag, status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv(x, j);
+                    }
+                    if (j + 1 < n_x[x]) issue_s(x, j + 1);
+                }
+                if (!ok) break;
+                umma_commit(bar(B_EMPTY(slot_of(2 * j + 1))));
+                if (next) umma_commit(bar(B_EMPTY(slot_of(2 * j + 2))));
             }
             // Tensor memory may be freed only after every issued MMA completed.
             umma_commit(bar(B_MMAFIN));
             volatile int no_abort = 0;
             mbar_wait_bounded(bar(B_MMAFIN), 0, &no_abort, status);
         }
-    } else {
+    } else if (warp < 8) {
         // ------------------------------------------------------------ softmax / correction / epilogue
+        regs_increase<kRegsSoftmax>();
+        const int x = warp >> 2;       // Q tile of this warp
         const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter+32) belong to this warp
-        const int r = quarter * 32 + lane;
-        const int i = q0 + r;
+        const int qx = q0 + x * kFwdBr;
+        const int i = qx + quarter * 32 + lane;
+        const int n_tiles = x == 0 ? nA : nB;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t s_addr = lane_base + C::tmem_s(x);
+        const uint32_t o_addr = lane_base + C::tmem_o(x);
         const int lim = causal ? min(i + (Nk - Nq), Nk - 1) : Nk - 1;  // last key row i may see
         const float sl2 = args.scale_log2;
-        float m = -INFINITY;  // running max of scale*log2(e)*s
-        float l = 0.f;        // running sum of 2^(.. - m)
+        float m = -INFINITY;  // running (possibly stale) max of scale*log2(e)*s
+        float l = 0.f;        // running sum of 2^(scale*log2(e)*s - m)
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
-            ok = mbar_wait_bounded(bar(B_SFULL(j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, status);
+            ok = mbar_wait_bounded(bar(B_SFULL(x)), (uint32_t)j & 1u, abort_flag, status);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t sbuf = lane_base + ((j & 1) ? C::kTmemS1 : C::kTmemS0);
             uint32_t sr[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(sbuf + 32 * c, sr[c]);
+            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(s_addr + 32 * c, sr[c]);
             tmem_wait_ld();
-            const bool masked = fwd_tile_needs_mask(j, q0, Nq, Nk, causal);
+            const bool masked = fwd_tile_needs_mask(j, qx, Nq, Nk, causal);
             if (masked) {
                 const int c0 = j * kFwdBc;
 #pragma unroll
@@ -251,61 +290,59 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             float mx = -INFINITY;
 #pragma unroll
             for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c >> 5][c & 31]));
-            const float m_new = fmaxf(m, mx * sl2);
-            const float m_d = (m_new == -INFINITY) ? 0.f : m_new;  // never subtract -inf from -inf
-            const float alpha = ex2_approx(m - m_d);
-            float rs = 0.f;
-            uint32_t ph[2][32], pl[2][32];
+            const float m_cand = fmaxf(m, mx * sl2);
+            const bool rescale = __any_sync(0xffffffffu, m_cand > m + kRescaleThreshold);
+            float alpha = 1.f;
+            if (rescale) {
+                const float m_new_d = (m_cand == -INFINITY) ? 0.f : m_cand;  // never subtract -inf from -inf
+                alpha = ex2_approx(m - m_new_d);
+                m = m_cand;
+            }
+            const float m_d = (m == -INFINITY) ? 0.f : m;
+            float rs0 = 0.f, rs1 = 0.f;
+            // P in chunks of 32 columns: 16 packed pairs each, stored as soon as they are
+            // ready (the whole S row is already in registers, so overwriting S is safe).
 #pragma unroll
-            for (int c = 0; c < 128; c += 2) {
-                const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -m_d));
-                const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c >> 5][(c + 1) & 31]), sl2, -m_d));
-                rs += p0 + p1;
-                const uint32_t h = PK::pack(p0, p1);
-                ph[c >> 6][(c >> 1) & 31] = h;
-                if (masked) {
-                    const float2 hf = PK::unpack(h);
-                    pl[c >> 6][(c >> 1) & 31] = PK::pack(p0 - hf.x, p1 - hf.y);
+            for (int c = 0; c < 4; ++c) {
+                uint32_t ph[16], pl[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), sl2, -m_d));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), sl2, -m_d));
+                    rs0 += p0;
+                    rs1 += p1;
+                    ph[e >> 1] = PK::pack(p0, p1);
+                    if (masked) {
+                        const float2 hf = PK::unpack(ph[e >> 1]);
+                        pl[e >> 1] = PK::pack(p0 - hf.x, p1 - hf.y);
+                    }
                 }
+                tmem_st_32x32b_x16(s_addr + 16 * c, ph);
+                if (masked) tmem_st_32x32b_x16(s_addr + C::kTmemPlo + 16 * c, pl);
             }
-            l = l * alpha + rs;
-            m = m_new;
-            if (j > 0) {
-                // P and O are free once the previous O += P V has completed.
-                ok = mbar_wait_bounded(bar(B_ODONE), (uint32_t)(j - 1) & 1u, abort_flag, status);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-            }
-            tmem_st_32x32b_x32(lane_base + C::kTmemP, ph[0]);
-            tmem_st_32x32b_x32(lane_base + C::kTmemP + 32, ph[1]);
-            if (masked) {
-                tmem_st_32x32b_x32(lane_base + C::kTmemPlo, pl[0]);
-                tmem_st_32x32b_x32(lane_base + C::kTmemPlo + 32, pl[1]);
-            }
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            l = l * alpha + (rs0 + rs1);
+            if (rescale && j > 0) {
+                // O_X holds PV_X(0..j-1), all complete (covered by the S_X(j) commit).
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t orow[32];
-                    tmem_ld_32x32b_x32(lane_base + C::kTmemO + 32 * c, orow);
+                    tmem_ld_32x32b_x32(o_addr + 32 * c, orow);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) orow[e] = __float_as_uint(__uint_as_float(orow[e]) * alpha);
-                    tmem_st_32x32b_x32(lane_base + C::kTmemO + 32 * c, orow);
+                    tmem_st_32x32b_x32(o_addr + 32 * c, orow);
                 }
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(B_PFULL(j & 1)));
+            mbar_arrive(bar(B_PFULL(x)));
         }
         if (ok && n_tiles > 0) {
-            ok = mbar_wait_bounded(bar(B_ODONE), (uint32_t)(n_tiles - 1) & 1u, abort_flag, status);
+            ok = mbar_wait_bounded(bar(B_OFINAL(x)), 0, abort_flag, status);
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
         }
-        if (ok) {
+        if (ok && __any_sync(0xffffffffu, i < Nq)) {
             // Epilogue: O = O~ / l (0 for a row that saw no key), LSE = m ln2 + ln l.
             const bool valid = i < Nq;
             const float inv = (l > 0.f) ? 1.f / l : 0.f;
@@ -314,7 +351,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t ov[32];
                 if (n_tiles > 0) {
-                    tmem_ld_32x32b_x32(lane_base + C::kTmemO + 32 * c, ov);
+                    tmem_ld_32x32b_x32(o_addr + 32 * c, ov);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
@@ -331,15 +368,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
             }
             if (valid && args.lse != nullptr) {
-                const float m_d = (m == -INFINITY) ? 0.f : m;
-                args.lse[(size_t)bh * Nq + i] = (l > 0.f) ? m_d * 0.69314718055994531f + logf(l) : -INFINITY;
+                const float m_fin = (m == -INFINITY) ? 0.f : m;
+                args.lse[(size_t)bh * Nq + i] = (l > 0.f) ? m_fin * 0.69314718055994531f + logf(l) : -INFINITY;
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 9) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
@@ -353,7 +390,7 @@ static cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, co
     auto kern = fa_fwd_kernel<D, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)BH, (unsigned)a.num_m, 1);
+    dim3 grid((unsigned)a.num_m, (unsigned)BH, 1);
     kern<<<grid, kFwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
     return cudaGetLastError();
 }

@@ -15,6 +15,8 @@ constexpr int kDevErrTimeout = 1;
 // lane per row) and 128 keys per K/V tile.
 constexpr int kFwdBr = 128;
 constexpr int kFwdBc = 128;
+// Q tiles per CTA of the fused forward (they ping-pong on the tensor core).
+constexpr int kFwdTilesPerCta = 2;
 // Keys per tile of the split-KV kernel; split lengths are multiples of it.
 constexpr int kDecBc = 64;
 constexpr int kMaxSplits = 256;
@@ -24,7 +26,7 @@ struct FwdArgs {
     float *lse;     // [BH, Nq] or nullptr
     int *status;    // device status word
     int Nq, Nk;
-    int num_m;      // ceil(Nq / kFwdBr)
+    int num_m;      // ceil(Nq / (kFwdTilesPerCta * kFwdBr)): row blocks per head
     int causal;
     float scale_log2;  // scale * log2(e)
 };

@@ -72,7 +72,7 @@ typedef enum {
 } fa_status;
 
 /*
- * Fused attention forward (one launch): one CTA per 128-row Q tile and head,
+ * Fused attention forward (one launch): one CTA per 256 query rows and head,
  * K/V tiles streamed by TMA, both GEMMs on tcgen05 tensor cores with fp32
  * accumulators in tensor memory, online softmax with deferred 1/l.  Under
  * causal masking, K/V tiles entirely above the diagonal are skipped and only
@@ -83,7 +83,8 @@ typedef enum {
  *   o        output [B, H, Nq, d], same dtype as the inputs.
  *   lse      output [B, H, Nq] fp32 (natural log of the scaled scores), or NULL.
  *   scale    score scale, normally 1/sqrt(d).
- * Returns FA_OK or one of the validation errors above.
+ * Returns FA_OK or one of the validation errors above, or FA_ERR_INVALID_ARG
+ * when B*H > 65535 (one grid dimension per head).
  */
 FA_API int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            int B, int H, int Nq, int Nk, int d, int causal, float scale,
