@@ -93,6 +93,58 @@ __device__ __forceinline__ int fwd_tile_count(int q0, int Nq, int Nk, int causal
     return kv_end > 0 ? (kv_end + kFwdBc - 1) / kFwdBc : 0;
 }
 
+// One online-softmax step for the S row held in `sr` (128 columns, fp32 bits):
+// optional causal/tail mask, (conditional) max update, p = 2^(s*c - m), row sum,
+// and P written back into the S columns as 16-bit pairs (plus the 16-bit
+// remainder on masked tiles).  Returns whether the warp moved its max (then
+// `alpha` is the factor O and l must be scaled by).
+template <bool MASKED, bool BF16>
+__device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[4][32], int c0, int lim, float sl2, float &m, float &l,
+                                             float &alpha, uint32_t s_addr) {
+    using PK = Pack<BF16>;
+    if (MASKED) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+            if (c0 + c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+    }
+    float mx[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(sr[0][e]);
+#pragma unroll
+    for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sr[c >> 5][c & 31]));
+    const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+    const float m_cand = fmaxf(m, mt * sl2);
+    const bool rescale = __any_sync(0xffffffffu, m_cand > m + kRescaleThreshold);
+    if (rescale) {
+        const float m_new_d = (m_cand == -INFINITY) ? 0.f : m_cand;  // never subtract -inf from -inf
+        alpha = ex2_approx(m - m_new_d);
+        m = m_cand;
+    }
+    const float m_d = (m == -INFINITY) ? 0.f : m;
+    float rs[4] = {0.f, 0.f, 0.f, 0.f};
+    // P in chunks of 32 columns: 16 packed pairs each, stored as soon as they are
+    // ready (the whole S row is already in registers, so overwriting S is safe).
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t ph[16], pl[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), sl2, -m_d));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), sl2, -m_d));
+            rs[(e >> 1) & 3] += p0 + p1;
+            ph[e >> 1] = PK::pack(p0, p1);
+            if (MASKED) {
+                const float2 hf = PK::unpack(ph[e >> 1]);
+                pl[e >> 1] = PK::pack(p0 - hf.x, p1 - hf.y);
+            }
+        }
+        tmem_st_32x32b_x16(s_addr + 16 * c, ph);
+        if (MASKED) tmem_st_32x32b_x16(s_addr + 64 + 16 * c, pl);
+    }
+    l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+    return rescale;
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -281,46 +333,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(s_addr + 32 * c, sr[c]);
             tmem_wait_ld();
             const bool masked = fwd_tile_needs_mask(j, qx, Nq, Nk, causal);
-            if (masked) {
-                const int c0 = j * kFwdBc;
-#pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c0 + c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
-            }
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c >> 5][c & 31]));
-            const float m_cand = fmaxf(m, mx * sl2);
-            const bool rescale = __any_sync(0xffffffffu, m_cand > m + kRescaleThreshold);
             float alpha = 1.f;
-            if (rescale) {
-                const float m_new_d = (m_cand == -INFINITY) ? 0.f : m_cand;  // never subtract -inf from -inf
-                alpha = ex2_approx(m - m_new_d);
-                m = m_cand;
+            bool rescale;
+            // Two instances of the same step, so the unmasked (common) tile carries
+            // no predicated mask or remainder instructions.
+            if (masked) {
+                rescale = softmax_tile<true, BF16>(sr, j * kFwdBc, lim, sl2, m, l, alpha, s_addr);
+            } else {
+                rescale = softmax_tile<false, BF16>(sr, 0, 0, sl2, m, l, alpha, s_addr);
             }
-            const float m_d = (m == -INFINITY) ? 0.f : m;
-            float rs0 = 0.f, rs1 = 0.f;
-            // P in chunks of 32 columns: 16 packed pairs each, stored as soon as they are
-            // ready (the whole S row is already in registers, so overwriting S is safe).
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t ph[16], pl[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), sl2, -m_d));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), sl2, -m_d));
-                    rs0 += p0;
-                    rs1 += p1;
-                    ph[e >> 1] = PK::pack(p0, p1);
-                    if (masked) {
-                        const float2 hf = PK::unpack(ph[e >> 1]);
-                        pl[e >> 1] = PK::pack(p0 - hf.x, p1 - hf.y);
-                    }
-                }
-                tmem_st_32x32b_x16(s_addr + 16 * c, ph);
-                if (masked) tmem_st_32x32b_x16(s_addr + C::kTmemPlo + 16 * c, pl);
-            }
-            l = l * alpha + (rs0 + rs1);
             if (rescale && j > 0) {
                 // O_X holds PV_X(0..j-1), all complete (covered by the S_X(j) commit).
 #pragma unroll
