@@ -109,10 +109,11 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[4][32], int c0, int 
     }
     float mx[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(sr[0][e]);
+    for (int e = 0; e < 8; ++e) mx[e] = fmax3(__uint_as_float(sr[0][2 * e]), __uint_as_float(sr[0][2 * e + 1]), -INFINITY);
 #pragma unroll
-    for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sr[c >> 5][c & 31]));
-    const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+    for (int c = 16; c < 128; c += 2)
+        mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], __uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[c >> 5][(c + 1) & 31]));
+    const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
     const float m_cand = fmaxf(m, mt * sl2);
     const bool rescale = __any_sync(0xffffffffu, m_cand > m + kRescaleThreshold);
     if (rescale) {
@@ -121,7 +122,9 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[4][32], int c0, int 
         m = m_cand;
     }
     const float m_d = (m == -INFINITY) ? 0.f : m;
-    float rs[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint64_t scale2 = f2_make(sl2, sl2);
+    const uint64_t shift2 = f2_make(-m_d, -m_d);
+    uint64_t rs2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
     // P in chunks of 32 columns: 16 packed pairs each, stored as soon as they are
     // ready (the whole S row is already in registers, so overwriting S is safe).
 #pragma unroll
@@ -129,9 +132,10 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[4][32], int c0, int 
         uint32_t ph[16], pl[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), sl2, -m_d));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), sl2, -m_d));
-            rs[(e >> 1) & 3] += p0 + p1;
+            const float2 xa = f2_split(ffma2(f2_make(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), scale2, shift2));
+            const float p0 = ex2_approx(xa.x);
+            const float p1 = ex2_approx(xa.y);
+            rs2[(e >> 1) & 1] = fadd2(rs2[(e >> 1) & 1], f2_make(p0, p1));
             ph[e >> 1] = PK::pack(p0, p1);
             if (MASKED) {
                 const float2 hf = PK::unpack(ph[e >> 1]);
@@ -141,6 +145,8 @@ __device__ __forceinline__ bool softmax_tile(uint32_t (&sr)[4][32], int c0, int 
         tmem_st_32x32b_x16(s_addr + 16 * c, ph);
         if (MASKED) tmem_st_32x32b_x16(s_addr + 64 + 16 * c, pl);
     }
+    const float2 r0 = f2_split(rs2[0]), r1 = f2_split(rs2[1]);
+    const float rs[4] = {r0.x, r0.y, r1.x, r1.y};
     l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
     return rescale;
 }
@@ -245,31 +251,37 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const int n_x[2] = {nA, nB};
             auto slot_of = [](int t) { return t % C::kStages; };
             auto par_of = [](int t) { return (uint32_t)(t / C::kStages) & 1u; };
+            // Descriptors are built once; per instruction only the address field of the
+            // low word moves (by a compile-time offset plus the slot offset).
+            constexpr uint32_t hi = sdesc_hi_sw128(1024);                    // 8 rows x 128 B per core group
+            const uint32_t q_lo = sdesc_lo(sb + C::kOffQ, 16);               // K-major: LBO unused
+            const uint32_t k_lo = sdesc_lo(sb + C::kOffRing, 16);
+            const uint32_t v_lo = sdesc_lo(sb + C::kOffRing, C::kKVBlockBytes);  // MN-major: LBO = 64-col block
             // S_X(j) = Q_X K_j^T: K-major A and B, 16 of the d columns per instruction.
             auto issue_s = [&](int x, int j) {
-                const uint32_t qa = sb + C::kOffQ + x * C::kQBytes;
-                const uint32_t ka = sb + C::kOffRing + slot_of(2 * j) * C::kTileBytes;
+                const uint32_t qx_lo = q_lo + x * (C::kQBytes >> 4);
+                const uint32_t kj_lo = k_lo + slot_of(2 * j) * (C::kTileBytes >> 4);
+                const uint32_t d_s = tmem + C::tmem_s(x);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off_q = (k >> 2) * C::kQBlockBytes + (k & 3) * 32;
-                    const uint32_t off_k = (k >> 2) * C::kKVBlockBytes + (k & 3) * 32;
-                    umma_ss(tmem + C::tmem_s(x), sdesc_sw128(qa + off_q, 16, 1024),
-                            sdesc_sw128(ka + off_k, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+                    const uint32_t off_q = ((k >> 2) * C::kQBlockBytes + (k & 3) * 32) >> 4;
+                    const uint32_t off_k = ((k >> 2) * C::kKVBlockBytes + (k & 3) * 32) >> 4;
+                    umma_ss_w(d_s, qx_lo + off_q, hi, kj_lo + off_k, hi, idesc_qk, k > 0 ? 1u : 0u);
                 }
                 umma_commit(bar(B_SFULL(x)));
             };
             // O_X += P_X(j) V_j: P from TMEM, V as an MN-major operand, 16 keys per instruction.
             auto issue_pv = [&](int x, int j) {
-                const uint32_t va = sb + C::kOffRing + slot_of(2 * j + 1) * C::kTileBytes;
+                const uint32_t vj_lo = v_lo + slot_of(2 * j + 1) * (C::kTileBytes >> 4);
+                const uint32_t d_o = tmem + C::tmem_o(x);
+                const uint32_t p_t = tmem + C::tmem_s(x);
 #pragma unroll
                 for (int k = 0; k < kFwdBc / 16; ++k)
-                    umma_ts(tmem + C::tmem_o(x), tmem + C::tmem_s(x) + 8 * k,
-                            sdesc_sw128(va + k * 2048, C::kKVBlockBytes, 1024), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+                    umma_ts_w(d_o, p_t + 8 * k, vj_lo + ((k * 2048) >> 4), hi, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
                 if (fwd_tile_needs_mask(j, q0 + x * kFwdBr, Nq, Nk, causal)) {
 #pragma unroll
                     for (int k = 0; k < kFwdBc / 16; ++k)
-                        umma_ts(tmem + C::tmem_o(x), tmem + C::tmem_s(x) + C::kTmemPlo + 8 * k,
-                                sdesc_sw128(va + k * 2048, C::kKVBlockBytes, 1024), idesc_pv, 1u);
+                        umma_ts_w(d_o, p_t + C::kTmemPlo + 8 * k, vj_lo + ((k * 2048) >> 4), hi, idesc_pv, 1u);
                 }
                 if (j == n_x[x] - 1) umma_commit(bar(B_OFINAL(x)));
             };
