@@ -35,10 +35,11 @@ FA_ERR_MISALIGNED = -3
 FA_ERR_WORKSPACE = -4
 FA_ERR_CUDA = -5
 FA_ERR_DEVICE_TIMEOUT = -6
+FA_ERR_SCRATCH_LIMIT = -7
 
 EXPORTS = ("fa_fwd", "fa_fwd_splitkv", "fa_splitkv_combine", "fa_splitkv_workspace_bytes",
            "fa_splitkv_num_splits", "fa_splitkv_split_len", "fa_get_device_status", "fa_status_string",
-           "fa_version")
+           "fa_version", "fa_fwd_splitkv_noalloc", "fa_splitkv_noalloc_capacity_bytes")
 
 _lock = threading.Lock()
 _lib = None
@@ -79,6 +80,10 @@ def load_library(path: str | None = None):
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_version.argtypes = []
         lib.fa_version.restype = i
+        lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
+        lib.fa_fwd_splitkv_noalloc.restype = i
+        lib.fa_splitkv_noalloc_capacity_bytes.argtypes = []
+        lib.fa_splitkv_noalloc_capacity_bytes.restype = sz
         if path is None:
             _lib = lib
         return lib
@@ -187,6 +192,22 @@ def fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None, num_s
                             workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_splitkv")
+    return out, lse
+
+
+def fwd_splitkv_noalloc(q, k, v, causal: bool = False, scale: float | None = None, num_splits: int = 0, out=None,
+                        lse=None, want_lse: bool = True, stream=None):
+    """Split-KV forward through ``fa_fwd_splitkv_noalloc``: the partials use the
+    library's built-in scratch, so no workspace is passed.  Returns (o, lse)."""
+    B, H, Nq, Nk, d = _check_qkv(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out, lse = _outputs(q, out, lse, B, H, Nq, want_lse)
+    lib = load_library()
+    rc = lib.fa_fwd_splitkv_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d,
+                                    int(bool(causal)), scale, _dtype_code(q), int(num_splits), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_splitkv_noalloc")
     return out, lse
 
 

@@ -17,6 +17,12 @@ namespace fa {
 // Per-device status word: kernels OR error bits into it (see kDevErrTimeout).
 __device__ int g_status_word;
 
+// Built-in scratch for fa_fwd_splitkv_noalloc: the split partials live here
+// instead of in a caller-provided workspace.  Every GPU that loads this library
+// holds these bytes until the process exits.
+constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_splitkv_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -29,6 +35,7 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+void *g_scratch_addr[kMaxDevices];  // device address of g_splitkv_scratch, looked up once per device
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int dev_state(DeviceState **out) {
@@ -120,6 +127,7 @@ const char *fa_status_string(int status) {
         case FA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         case FA_ERR_CUDA: return "CUDA runtime error";
         case FA_ERR_DEVICE_TIMEOUT: return "a device-side bounded wait ran out";
+        case FA_ERR_SCRATCH_LIMIT: return "split partials exceed the built-in 16 MiB scratch of fa_fwd_splitkv_noalloc";
         default: return "unknown status";
     }
 }
@@ -248,6 +256,60 @@ int fa_get_device_status(fa_stream_t stream) {
     }
     if (cudaPeekAtLastError() != cudaSuccess) return FA_ERR_CUDA;
     return FA_OK;
+}
+
+size_t fa_splitkv_noalloc_capacity_bytes(void) { return kNoAllocScratchBytes; }
+
+int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq,
+                           int Nk, int d, int causal, float scale, fa_dtype dtype, int num_splits, fa_stream_t stream) {
+    int rc = check_common(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, dtype);
+    if (rc != FA_OK) return rc;
+    if (num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+    DeviceState *st = nullptr;
+    if ((rc = dev_state(&st)) != FA_OK) return rc;
+    const long long rows = (long long)B * H * Nq;
+    if (num_splits <= 0) num_splits = auto_splits(st->num_sms, rows, Nk);
+    if ((long long)num_splits * rows > INT32_MAX) return FA_ERR_INVALID_ARG;
+    const size_t o_bytes = align256((size_t)num_splits * rows * d * sizeof(float));
+    const size_t need = o_bytes + align256((size_t)num_splits * rows * sizeof(float));
+    if (need > kNoAllocScratchBytes) return FA_ERR_SCRATCH_LIMIT;
+    // The scratch array's host-side name is not a device address: look the address
+    // up once per device, with that device current, and pass it to the kernels.
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_scratch_addr[dev] == nullptr) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_splitkv_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
+            g_scratch_addr[dev] = p;
+        }
+        scratch = g_scratch_addr[dev];
+    }
+    const bool bf16 = dtype == FA_BF16;
+    const int BH = B * H;
+    CUtensorMap tk, tv;
+    if (make_map(&tk, k, bf16, d, Nk, BH, kDecBc) != FA_OK || make_map(&tv, v, bf16, d, Nk, BH, kDecBc) != FA_OK)
+        return FA_ERR_CUDA;
+    float *o_part = static_cast<float *>(scratch);
+    float *lse_part = reinterpret_cast<float *>(static_cast<char *>(scratch) + o_bytes);
+    SplitArgs a;
+    a.q = q;
+    a.o_part = o_part;
+    a.lse_part = lse_part;
+    a.status = st->status;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.BH = BH;
+    a.num_splits = num_splits;
+    a.split_len = fa_splitkv_split_len(Nk, num_splits);
+    a.causal = causal;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_splitkv(d, bf16, tk, tv, a, s);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+    return fa_splitkv_combine(o_part, lse_part, o, lse, num_splits, B, H, Nq, d, dtype, stream);
 }
 
 }  // extern "C"

@@ -68,7 +68,8 @@ typedef enum {
     FA_ERR_MISALIGNED = -3,
     FA_ERR_WORKSPACE = -4,
     FA_ERR_CUDA = -5,
-    FA_ERR_DEVICE_TIMEOUT = -6
+    FA_ERR_DEVICE_TIMEOUT = -6,
+    FA_ERR_SCRATCH_LIMIT = -7
 } fa_status;
 
 /*
@@ -143,6 +144,38 @@ FA_API int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, 
 FA_API int fa_splitkv_combine(const float *o_part, const float *lse_part, void *o, float *lse,
                        int num_splits, int B, int H, int Nq, int d, fa_dtype dtype,
                        fa_stream_t stream);
+
+/*
+ * Split-KV attention forward that allocates nothing and needs no workspace.
+ * (No counterpart in the source pages: this is a library convenience.)
+ *
+ * For callers that cannot allocate device memory at the point of the call --
+ * code running inside a CUDA graph capture or a memory-pool-less runtime, a
+ * host that must not grow its footprint after start-up, a caller without a
+ * device allocator of its own -- this variant keeps the split partials in a
+ * fixed scratch array built into the library (a file-scope __device__ array of
+ * fa_splitkv_noalloc_capacity_bytes() = 16 MiB, held on every GPU that loads
+ * the library until the process exits).  It calls no cudaMalloc or cudaFree.
+ *
+ * Arguments and results are those of fa_fwd_splitkv without the workspace;
+ * the caller still provides q, k, v, o and lse.  The partials need
+ * num_splits * B * H * Nq * (d + 1) * 4 bytes (each of the two regions rounded
+ * up to 256 bytes); a problem that does not fit returns FA_ERR_SCRATCH_LIMIT
+ * before anything is launched (use fewer splits, or fa_fwd_splitkv).
+ *
+ * The first call on a device looks up the scratch array's device address with
+ * that device current; make that first call before any stream capture.  All
+ * calls in the process share the one array and every call overwrites it, so
+ * two calls whose kernels overlap on the GPU (different streams without
+ * ordering between them) race and give wrong results.  Nothing in the scratch
+ * needs clearing: every partial is written before the combine reads it.
+ */
+FA_API int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                                  int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                                  fa_dtype dtype, int num_splits, fa_stream_t stream);
+
+/* Bytes of the built-in scratch used by fa_fwd_splitkv_noalloc (16 MiB). */
+FA_API size_t fa_splitkv_noalloc_capacity_bytes(void);
 
 /*
  * Synchronises `stream`, then returns FA_ERR_DEVICE_TIMEOUT if any kernel of
