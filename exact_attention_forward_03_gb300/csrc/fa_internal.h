@@ -11,11 +11,10 @@ namespace fa {
 // Device-side error bits OR-ed into the per-device status word.
 constexpr int kDevErrTimeout = 1;
 
-// Tile shape of the fused forward kernel: 128 query rows per CTA (one TMEM
-// lane per row) and 128 keys per K/V tile.
+// Tile shape of the fused forward kernel: 128 query rows per Q tile (one TMEM
+// lane per row), two Q tiles per CTA, 64 keys per K/V step.
 constexpr int kFwdBr = 128;
-constexpr int kFwdBc = 128;
-// Q tiles per CTA of the fused forward (they ping-pong on the tensor core).
+constexpr int kFwdBc = 64;
 constexpr int kFwdTilesPerCta = 2;
 // Keys per tile of the split-KV kernel; split lengths are multiples of it.
 constexpr int kDecBc = 64;
