@@ -18,19 +18,22 @@
 //              (64 keys each) through a ring of shared-memory slots
 //   warp 9     owns tensor memory; one lane issues every tcgen05.mma
 //
-// Tensor memory (512 columns), for each tile X: S_X (64 fp32 columns), P_X
-// (64 keys as 16-bit pairs, 32 columns), P_lo_X (32 columns) and O_X (d fp32
-// columns).  Because P has its own columns, S_X(j+1) = Q_X K_{j+1}^T is issued
-// as soon as the softmax warps have read S_X(j) into registers, before
+// Tensor memory (512 columns), for each tile X: S_X (64 fp32 columns), two P
+// buffers P_X[0], P_X[1] (64 keys as 16-bit pairs, 32 columns each) and O_X (d
+// fp32 columns).  Because P has its own columns, S_X(j+1) = Q_X K_{j+1}^T is
+// issued as soon as the softmax warps have read S_X(j) into registers, before
 // O_X += P_X(j) V_j: the tensor core computes the next scores while the
-// softmax of the current step runs, and the two tiles keep it fed.  The
-// softmax waits only for O_X += P_X(j-1) V_{j-1} (which reads P_X) before it
-// writes P_X(j).  MMA order per step j: S_A(j+1), S_B(j+1), PV_A(j), PV_B(j).
+// softmax of the current step runs, and the two tiles keep it fed.  Step j
+// writes P_X[j % 2], so the softmax of step j waits only for the MMA that read
+// that buffer two steps earlier.  MMA order per step j: S_A(j+1), S_B(j+1),
+// PV_A(j), PV_B(j).
 //
-// On tiles that need a mask, P is written as a 16-bit head P_X plus a 16-bit
-// remainder P_lo_X = P - P_X and both are multiplied into O: rows near the
-// diagonal see few keys, so one 16-bit rounding of their few large weights
-// would otherwise dominate their error.
+// On steps that need a mask, P is written as a 16-bit head P plus a 16-bit
+// remainder P - P_head in the other buffer, and both are multiplied into O:
+// rows near the diagonal see few keys, so one 16-bit rounding of their few
+// large weights would otherwise dominate their error.  Every MMA group that
+// reads a P buffer commits to that buffer's barrier, and both sides count those
+// uses the same way, so the softmax always knows which phase to wait for.
 //
 // The rescale of O by alpha = 2^(m_old - m_new) is done only when the row max
 // of some row in the warp grew by more than 2^8: otherwise m stays and p may
@@ -61,15 +64,14 @@ struct FwdCfg {
     static constexpr int kOffQ = 0;                      // Q_A, then Q_B
     static constexpr int kOffRing = kFwdTilesPerCta * kQBytes;
     static constexpr int kOffBar = kOffRing + kStages * kTileBytes;
-    // barriers: q_full, full[S], empty[S], s_full[2], s_free[2], p_full[2], pv_done[2], o_final[2], mma_fin
-    static constexpr int kNumBars = 1 + 2 * kStages + 5 * 2 + 1;
+    // barriers: q_full, full[S], empty[S], s_full[2], s_free[2], p_full[2], p_read[2][2], o_final[2], mma_fin
+    static constexpr int kNumBars = 1 + 2 * kStages + 6 * 2 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
     static constexpr uint32_t kTmemCols = 512;
     __device__ static constexpr uint32_t tmem_s(int x) { return 64u * x; }          // [0,64), [64,128)
-    __device__ static constexpr uint32_t tmem_p(int x) { return 128u + 32u * x; }   // [128,160), [160,192)
-    __device__ static constexpr uint32_t tmem_plo(int x) { return 192u + 32u * x; } // [192,224), [224,256)
+    __device__ static constexpr uint32_t tmem_p(int x, int b) { return 128u + 64u * x + 32u * b; }  // [128,256)
     __device__ static constexpr uint32_t tmem_o(int x) { return 256u + (uint32_t)D * x; }
 };
 
@@ -189,9 +191,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     auto B_SFULL = [](int x) { return 1 + 2 * C::kStages + x; };
     auto B_SFREE = [](int x) { return 3 + 2 * C::kStages + x; };
     auto B_PFULL = [](int x) { return 5 + 2 * C::kStages + x; };
-    auto B_PVDONE = [](int x) { return 7 + 2 * C::kStages + x; };
-    auto B_OFINAL = [](int x) { return 9 + 2 * C::kStages + x; };
-    constexpr int B_MMAFIN = 11 + 2 * C::kStages;
+    auto B_PREAD = [](int x, int b) { return 7 + 2 * C::kStages + 2 * x + b; };  // an MMA group read P_X[b]
+    auto B_OFINAL = [](int x) { return 11 + 2 * C::kStages + x; };
+    constexpr int B_MMAFIN = 13 + 2 * C::kStages;
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
     int *status = args.status;
@@ -206,7 +208,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_init(bar(B_SFULL(x)), 1);
             mbar_init(bar(B_SFREE(x)), 128);
             mbar_init(bar(B_PFULL(x)), 128);
-            mbar_init(bar(B_PVDONE(x)), 1);
+            mbar_init(bar(B_PREAD(x, 0)), 1);
+            mbar_init(bar(B_PREAD(x, 1)), 1);
             mbar_init(bar(B_OFINAL(x)), 1);
         }
         mbar_init(bar(B_MMAFIN), 1);
@@ -281,20 +284,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
                 umma_commit(bar(B_SFULL(x)));
             };
-            // O_X += P_X(j) V_j: P from TMEM, V as an MN-major operand, 16 keys per instruction.
+            // O_X += P_X(j) V_j: P from TMEM buffer j % 2 (the remainder, on masked steps,
+            // from the other buffer), V as an MN-major operand, 16 keys per instruction.
             auto issue_pv = [&](int x, int j) {
                 const uint32_t vj_lo = v_lo + slot_of(2 * j + 1) * (C::kTileBytes >> 4);
                 const uint32_t d_o = tmem + C::tmem_o(x);
+                const int b = j & 1;
 #pragma unroll
                 for (int k = 0; k < kFwdBc / 16; ++k)
-                    umma_ts_w(d_o, tmem + C::tmem_p(x) + 8 * k, vj_lo + ((k * 2048) >> 4), hi, idesc_pv,
+                    umma_ts_w(d_o, tmem + C::tmem_p(x, b) + 8 * k, vj_lo + ((k * 2048) >> 4), hi, idesc_pv,
                               (j > 0 || k > 0) ? 1u : 0u);
+                umma_commit(bar(B_PREAD(x, b)));
                 if (fwd_tile_needs_mask(j, q0 + x * kFwdBr, Nq, Nk, causal)) {
 #pragma unroll
                     for (int k = 0; k < kFwdBc / 16; ++k)
-                        umma_ts_w(d_o, tmem + C::tmem_plo(x) + 8 * k, vj_lo + ((k * 2048) >> 4), hi, idesc_pv, 1u);
+                        umma_ts_w(d_o, tmem + C::tmem_p(x, b ^ 1) + 8 * k, vj_lo + ((k * 2048) >> 4), hi, idesc_pv, 1u);
+                    umma_commit(bar(B_PREAD(x, b ^ 1)));
                 }
-                umma_commit(bar(B_PVDONE(x)));
                 if (j == n_x[x] - 1) umma_commit(bar(B_OFINAL(x)));
             };
             bool ok = mbar_wait_bounded(bar(B_QFULL), 0, abort_flag, status) &&
@@ -346,13 +352,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int n_tiles = x == 0 ? nA : nB;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const uint32_t s_addr = lane_base + C::tmem_s(x);
-        const uint32_t p_addr = lane_base + C::tmem_p(x);
-        const uint32_t plo_addr = lane_base + C::tmem_plo(x);
         const uint32_t o_addr = lane_base + C::tmem_o(x);
         const int lim = causal ? min(i + (Nk - Nq), Nk - 1) : Nk - 1;  // last key row i may see
         const float sl2 = args.scale_log2;
         float m = -INFINITY;  // running (possibly stale) max of scale*log2(e)*s
         float l = 0.f;        // running sum of 2^(scale*log2(e)*s - m)
+        int reads[2] = {0, 0};  // MMA groups issued so far that read P_X[0] / P_X[1]
+        // Wait until every MMA group that read P_X[b] so far has completed.
+        auto wait_p_free = [&](int b) -> bool {
+            if (reads[b] == 0) return true;
+            return __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_PREAD(x, b)), (uint32_t)(reads[b] - 1) & 1u,
+                                                              abort_flag, status));
+        };
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_SFULL(x)), (uint32_t)j & 1u, abort_flag, status));
@@ -374,20 +385,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 rescale = softmax_step<true, BF16>(sr, j * kFwdBc, lim, sl2, m, l, alpha, ph, pl);
             else
                 rescale = softmax_step<false, BF16>(sr, 0, 0, sl2, m, l, alpha, ph, pl);
-            if (j > 0) {
-                // P_X and O_X are free once O_X += P_X(j-1) V_{j-1} has completed.
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait_bounded(bar(B_PVDONE(x)), (uint32_t)(j - 1) & 1u, abort_flag, status));
-                if (!ok) break;
-                tc_fence_after();
-            }
+            const int b = j & 1;
+            // P_X[b] (and on masked steps P_X[b^1]) must no longer be read by an earlier
+            // MMA group; a rescale of O_X needs every earlier group complete (the latest
+            // one read P_X[b^1]).
+            ok = wait_p_free(b) && ((!masked && !(rescale && j > 0)) || wait_p_free(b ^ 1));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t p_addr = lane_base + C::tmem_p(x, b);
             tmem_st_32x32b_x16(p_addr, *reinterpret_cast<uint32_t(*)[16]>(&ph[0]));
             tmem_st_32x32b_x16(p_addr + 16, *reinterpret_cast<uint32_t(*)[16]>(&ph[16]));
             if (masked) {
+                const uint32_t plo_addr = lane_base + C::tmem_p(x, b ^ 1);
                 tmem_st_32x32b_x16(plo_addr, *reinterpret_cast<uint32_t(*)[16]>(&pl[0]));
                 tmem_st_32x32b_x16(plo_addr + 16, *reinterpret_cast<uint32_t(*)[16]>(&pl[16]));
             }
             if (rescale && j > 0) rescale_o<D>(o_addr, alpha);  // O_X holds PV_X(0..j-1), all complete
+            reads[b] += 1;
+            if (masked) reads[b ^ 1] += 1;
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(B_PFULL(x)));
