@@ -64,8 +64,8 @@ struct FwdCfg {
     static constexpr int kOffQ = 0;                      // Q_A, then Q_B
     static constexpr int kOffRing = kFwdTilesPerCta * kQBytes;
     static constexpr int kOffBar = kOffRing + kStages * kTileBytes;
-    // barriers: q_full, full[S], empty[S], s_full[2], s_free[2], p_full[2], p_read[2][2], o_final[2], mma_fin
-    static constexpr int kNumBars = 1 + 2 * kStages + 6 * 2 + 1;
+    // barriers: q_full, full[S], empty[S], s_full[2], s_free[2], p_full[2][2], p_read[2][2], o_final[2], mma_fin
+    static constexpr int kNumBars = 1 + 2 * kStages + 7 * 2 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -190,10 +190,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     auto B_EMPTY = [](int s) { return 1 + C::kStages + s; };
     auto B_SFULL = [](int x) { return 1 + 2 * C::kStages + x; };
     auto B_SFREE = [](int x) { return 3 + 2 * C::kStages + x; };
-    auto B_PFULL = [](int x) { return 5 + 2 * C::kStages + x; };
-    auto B_PREAD = [](int x, int b) { return 7 + 2 * C::kStages + 2 * x + b; };  // an MMA group read P_X[b]
-    auto B_OFINAL = [](int x) { return 11 + 2 * C::kStages + x; };
-    constexpr int B_MMAFIN = 13 + 2 * C::kStages;
+    // P_X[b] written: one barrier per buffer, so the softmax (which may run a step
+    // ahead of the MMA warp) can never complete a phase twice before it is seen.
+    auto B_PFULL = [](int x, int b) { return 5 + 2 * C::kStages + 2 * x + b; };
+    auto B_PREAD = [](int x, int b) { return 9 + 2 * C::kStages + 2 * x + b; };  // an MMA group read P_X[b]
+    auto B_OFINAL = [](int x) { return 13 + 2 * C::kStages + x; };
+    constexpr int B_MMAFIN = 15 + 2 * C::kStages;
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
     int *status = args.status;
@@ -207,7 +209,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int x = 0; x < 2; ++x) {
             mbar_init(bar(B_SFULL(x)), 1);
             mbar_init(bar(B_SFREE(x)), 128);
-            mbar_init(bar(B_PFULL(x)), 128);
+            mbar_init(bar(B_PFULL(x, 0)), 128);
+            mbar_init(bar(B_PFULL(x, 1)), 128);
             mbar_init(bar(B_PREAD(x, 0)), 1);
             mbar_init(bar(B_PREAD(x, 1)), 1);
             mbar_init(bar(B_OFINAL(x)), 1);
@@ -329,7 +332,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 ok = mbar_wait_bounded(bar(B_FULL(slot_of(2 * j + 1))), par_of(2 * j + 1), abort_flag, status);
                 for (int x = 0; ok && x < 2; ++x) {
                     if (j < n_x[x]) {
-                        ok = mbar_wait_bounded(bar(B_PFULL(x)), (uint32_t)j & 1u, abort_flag, status);
+                        ok = mbar_wait_bounded(bar(B_PFULL(x, j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, status);
                         if (!ok) break;
                         tc_fence_after();
                         issue_pv(x, j);
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (masked) reads[b ^ 1] += 1;
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(B_PFULL(x)));
+            mbar_arrive(bar(B_PFULL(x, b)));
         }
         if (ok && n_tiles > 0) {
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_OFINAL(x)), 0, abort_flag, status));
