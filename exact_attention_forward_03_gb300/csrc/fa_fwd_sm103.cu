@@ -14,8 +14,8 @@
 // Roles (warp specialisation, 10 warps):
 //   warps 0-3  softmax of Q tile A, one thread per query row (TMEM lane = row)
 //   warps 4-7  softmax of Q tile B
-//   warp 8     TMA producer: both Q tiles once, then K_0, V_0, K_1, V_1, ...
-//              (64 keys each) through a ring of shared-memory slots
+//   warp 8     TMA producer: both Q tiles and K_0 once, then one ring stage per
+//              step j holding V_j and K_{j+1} (64 keys each)
 //   warp 9     owns tensor memory; one lane issues every tcgen05.mma
 //
 // Tensor memory (512 columns), for each tile X: S_X (64 fp32 columns), two P
@@ -34,6 +34,12 @@
 // large weights would otherwise dominate their error.  Every MMA group that
 // reads a P buffer commits to that buffer's barrier, and both sides count those
 // uses the same way, so the softmax always knows which phase to wait for.
+//
+// The two tiles share the barriers of the per-step handshakes (S ready, S read,
+// P ready): the MMA warp waits once per step for both tiles, which keeps its
+// serial bookkeeping between MMA groups short.  A tile with fewer steps than
+// its partner keeps arriving on those barriers, paced by "S ready", until the
+// partner is done.
 //
 // The rescale of O by alpha = 2^(m_old - m_new) is done only when the row max
 // of some row in the warp grew by more than 2^8: otherwise m stays and p may
@@ -60,12 +66,14 @@ struct FwdCfg {
     static constexpr int kKVBlockBytes = kFwdBc * 128;   // one 64-column block of a K/V tile
     static constexpr int kQBytes = kFwdBr * D * 2;       // one Q tile
     static constexpr int kTileBytes = kFwdBc * D * 2;    // one K or V tile
-    static constexpr int kStages = (D == 128) ? 8 : 16;
+    static constexpr int kStages = (D == 128) ? 4 : 8;  // ring stages of (V_j, K_{j+1})
+    static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kOffQ = 0;                      // Q_A, then Q_B
-    static constexpr int kOffRing = kFwdTilesPerCta * kQBytes;
-    static constexpr int kOffBar = kOffRing + kStages * kTileBytes;
-    // barriers: q_full, full[S], empty[S], s_full[2], s_free[2], p_full[2][2], p_read[2][2], o_final[2], mma_fin
-    static constexpr int kNumBars = 1 + 2 * kStages + 7 * 2 + 1;
+    static constexpr int kOffK0 = kFwdTilesPerCta * kQBytes;
+    static constexpr int kOffRing = kOffK0 + kTileBytes;
+    static constexpr int kOffBar = kOffRing + kStages * kStageBytes;
+    // barriers: q_full, full[S], empty[S], s_full, s_free, p_full[2], p_read[2][2], o_final[2], mma_fin
+    static constexpr int kNumBars = 1 + 2 * kStages + 1 + 1 + 2 + 4 + 2 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -188,14 +196,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     constexpr int B_QFULL = 0;
     auto B_FULL = [](int s) { return 1 + s; };
     auto B_EMPTY = [](int s) { return 1 + C::kStages + s; };
-    auto B_SFULL = [](int x) { return 1 + 2 * C::kStages + x; };
-    auto B_SFREE = [](int x) { return 3 + 2 * C::kStages + x; };
-    // P_X[b] written: one barrier per buffer, so the softmax (which may run a step
-    // ahead of the MMA warp) can never complete a phase twice before it is seen.
-    auto B_PFULL = [](int x, int b) { return 5 + 2 * C::kStages + 2 * x + b; };
-    auto B_PREAD = [](int x, int b) { return 9 + 2 * C::kStages + 2 * x + b; };  // an MMA group read P_X[b]
-    auto B_OFINAL = [](int x) { return 13 + 2 * C::kStages + x; };
-    constexpr int B_MMAFIN = 15 + 2 * C::kStages;
+    constexpr int B_SFULL = 1 + 2 * C::kStages;  // S_A(j), S_B(j) ready
+    constexpr int B_SFREE = 2 + 2 * C::kStages;  // both tiles have read S(j)
+    // P[b] written by both tiles: one barrier per buffer, so the softmax (which may
+    // run a step ahead of the MMA warp) can never complete a phase twice unseen.
+    auto B_PFULL = [](int b) { return 3 + 2 * C::kStages + b; };
+    auto B_PREAD = [](int x, int b) { return 5 + 2 * C::kStages + 2 * x + b; };  // an MMA group read P_X[b]
+    auto B_OFINAL = [](int x) { return 9 + 2 * C::kStages + x; };
+    constexpr int B_MMAFIN = 11 + 2 * C::kStages;
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
     int *status = args.status;
@@ -206,11 +214,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_init(bar(B_FULL(s)), 1);
             mbar_init(bar(B_EMPTY(s)), 1);
         }
+        mbar_init(bar(B_SFULL), 1);
+        mbar_init(bar(B_SFREE), 256);
+        mbar_init(bar(B_PFULL(0)), 256);
+        mbar_init(bar(B_PFULL(1)), 256);
         for (int x = 0; x < 2; ++x) {
-            mbar_init(bar(B_SFULL(x)), 1);
-            mbar_init(bar(B_SFREE(x)), 128);
-            mbar_init(bar(B_PFULL(x, 0)), 128);
-            mbar_init(bar(B_PFULL(x, 1)), 128);
             mbar_init(bar(B_PREAD(x, 0)), 1);
             mbar_init(bar(B_PREAD(x, 1)), 1);
             mbar_init(bar(B_OFINAL(x)), 1);
@@ -236,21 +244,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && n_max > 0) {
             uint32_t pend_mask = 0, pend_par = 0;
-            mbar_arrive_expect_tx(bar(B_QFULL), kFwdTilesPerCta * C::kQBytes);
+            mbar_arrive_expect_tx(bar(B_QFULL), kFwdTilesPerCta * C::kQBytes + C::kTileBytes);
             for (int x = 0; x < kFwdTilesPerCta; ++x)
                 for (int b = 0; b < C::kBlocks; ++b)
                     tma_load_3d(sb + C::kOffQ + x * C::kQBytes + b * C::kQBlockBytes, &tmQ, b * 64,
                                 q0 + x * kFwdBr, bh, bar(B_QFULL));
-            for (int t = 0; t < 2 * n_max; ++t) {
-                const int s = t % C::kStages;
-                const uint32_t it = (uint32_t)(t / C::kStages);
+            for (int b = 0; b < C::kBlocks; ++b)
+                tma_load_3d(sb + C::kOffK0 + b * C::kKVBlockBytes, &tmK, b * 64, 0, bh, bar(B_QFULL));
+            for (int j = 0; j < n_max; ++j) {
+                // stage j % kStages: V_j, then K_{j+1} (absent on the last step)
+                const int s = j % C::kStages;
+                const uint32_t it = (uint32_t)(j / C::kStages);
                 if (!mbar_wait_bounded(bar(B_EMPTY(s)), (it & 1u) ^ 1u, abort_flag, status)) break;
-                mbar_arrive_expect_tx(bar(B_FULL(s)), C::kTileBytes);
-                const CUtensorMap *map = (t & 1) ? &tmV : &tmK;
-                const int y = (t >> 1) * kFwdBc;
-                const uint32_t dst = sb + C::kOffRing + s * C::kTileBytes;
+                const bool next = j + 1 < n_max;
+                mbar_arrive_expect_tx(bar(B_FULL(s)), next ? 2 * C::kTileBytes : C::kTileBytes);
+                const uint32_t dst = sb + C::kOffRing + s * C::kStageBytes;
                 for (int b = 0; b < C::kBlocks; ++b)
-                    tma_load_3d(dst + b * C::kKVBlockBytes, map, b * 64, y, bh, bar(B_FULL(s)));
+                    tma_load_3d(dst + b * C::kKVBlockBytes, &tmV, b * 64, j * kFwdBc, bh, bar(B_FULL(s)));
+                if (next)
+                    for (int b = 0; b < C::kBlocks; ++b)
+                        tma_load_3d(dst + C::kTileBytes + b * C::kKVBlockBytes, &tmK, b * 64, (j + 1) * kFwdBc, bh,
+                                    bar(B_FULL(s)));
                 pend_mask |= 1u << s;
                 pend_par = (pend_par & ~(1u << s)) | ((it & 1u) << s);
             }
@@ -265,32 +279,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (lane == 0 && n_max > 0) {
             constexpr uint32_t idesc_qk = idesc_f16(128, kFwdBc, BF16, false);
             constexpr uint32_t idesc_pv = idesc_f16(128, D, BF16, true);
-            const int n_x[2] = {nA, nB};
-            auto slot_of = [](int t) { return t % C::kStages; };
-            auto par_of = [](int t) { return (uint32_t)(t / C::kStages) & 1u; };
             // Descriptors are built once; per instruction only the address field of the
-            // low word moves (by a compile-time offset plus the slot offset).
+            // low word moves (by a compile-time offset plus the stage offset).
             constexpr uint32_t hi = sdesc_hi_sw128(1024);                        // 8 rows x 128 B per core group
             const uint32_t q_lo = sdesc_lo(sb + C::kOffQ, 16);                   // K-major: LBO unused
-            const uint32_t k_lo = sdesc_lo(sb + C::kOffRing, 16);
-            const uint32_t v_lo = sdesc_lo(sb + C::kOffRing, C::kKVBlockBytes);  // MN-major: LBO = 64-col block
-            // S_X(j) = Q_X K_j^T: K-major A and B, N = 64 keys, 16 of the d columns per instruction.
-            auto issue_s = [&](int x, int j) {
+            const uint32_t k0_lo = sdesc_lo(sb + C::kOffK0, 16);
+            const uint32_t ring_k_lo = sdesc_lo(sb + C::kOffRing + C::kTileBytes, 16);
+            const uint32_t ring_v_lo = sdesc_lo(sb + C::kOffRing, C::kKVBlockBytes);  // MN-major: LBO = 64-col block
+            // S_X = Q_X K^T for the K tile whose descriptor low word is k_lo: K-major A and
+            // B, N = 64 keys, 16 of the d columns per instruction.
+            auto issue_s = [&](int x, uint32_t k_lo) {
                 const uint32_t qx_lo = q_lo + x * (C::kQBytes >> 4);
-                const uint32_t kj_lo = k_lo + slot_of(2 * j) * (C::kTileBytes >> 4);
                 const uint32_t d_s = tmem + C::tmem_s(x);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off_q = ((k >> 2) * C::kQBlockBytes + (k & 3) * 32) >> 4;
                     const uint32_t off_k = ((k >> 2) * C::kKVBlockBytes + (k & 3) * 32) >> 4;
-                    umma_ss_w(d_s, qx_lo + off_q, hi, kj_lo + off_k, hi, idesc_qk, k > 0 ? 1u : 0u);
+                    umma_ss_w(d_s, qx_lo + off_q, hi, k_lo + off_k, hi, idesc_qk, k > 0 ? 1u : 0u);
                 }
-                umma_commit(bar(B_SFULL(x)));
             };
             // O_X += P_X(j) V_j: P from TMEM buffer j % 2 (the remainder, on masked steps,
             // from the other buffer), V as an MN-major operand, 16 keys per instruction.
-            auto issue_pv = [&](int x, int j) {
-                const uint32_t vj_lo = v_lo + slot_of(2 * j + 1) * (C::kTileBytes >> 4);
+            auto issue_pv = [&](int x, int j, uint32_t vj_lo) {
                 const uint32_t d_o = tmem + C::tmem_o(x);
                 const int b = j & 1;
 #pragma unroll
@@ -304,42 +314,35 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         umma_ts_w(d_o, tmem + C::tmem_p(x, b ^ 1) + 8 * k, vj_lo + ((k * 2048) >> 4), hi, idesc_pv, 1u);
                     umma_commit(bar(B_PREAD(x, b ^ 1)));
                 }
-                if (j == n_x[x] - 1) umma_commit(bar(B_OFINAL(x)));
+                if (j == (x == 0 ? nA : nB) - 1) umma_commit(bar(B_OFINAL(x)));
             };
-            bool ok = mbar_wait_bounded(bar(B_QFULL), 0, abort_flag, status) &&
-                      mbar_wait_bounded(bar(B_FULL(slot_of(0))), par_of(0), abort_flag, status);
+            bool ok = mbar_wait_bounded(bar(B_QFULL), 0, abort_flag, status);
             if (ok) {
                 tc_fence_after();
-                if (nA > 0) issue_s(0, 0);
-                if (nB > 0) issue_s(1, 0);
-                umma_commit(bar(B_EMPTY(slot_of(0))));
+                if (nA > 0) issue_s(0, k0_lo);
+                if (nB > 0) issue_s(1, k0_lo);
+                umma_commit(bar(B_SFULL));
             }
             for (int j = 0; ok && j < n_max; ++j) {
-                // Next scores first: S_X(j+1) may overwrite S_X once the softmax has read S_X(j).
-                if (j + 1 < n_max) {
-                    ok = mbar_wait_bounded(bar(B_FULL(slot_of(2 * j + 2))), par_of(2 * j + 2), abort_flag, status);
-                    for (int x = 0; ok && x < 2; ++x) {
-                        if (j + 1 < n_x[x]) {
-                            ok = mbar_wait_bounded(bar(B_SFREE(x)), (uint32_t)j & 1u, abort_flag, status);
-                            if (!ok) break;
-                            tc_fence_after();
-                            issue_s(x, j + 1);
-                        }
-                    }
-                    if (!ok) break;
-                    umma_commit(bar(B_EMPTY(slot_of(2 * j + 2))));
-                }
-                ok = mbar_wait_bounded(bar(B_FULL(slot_of(2 * j + 1))), par_of(2 * j + 1), abort_flag, status);
-                for (int x = 0; ok && x < 2; ++x) {
-                    if (j < n_x[x]) {
-                        ok = mbar_wait_bounded(bar(B_PFULL(x, j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, status);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_pv(x, j);
-                    }
-                }
+                const int s = j % C::kStages;
+                const uint32_t stage_off = s * (C::kStageBytes >> 4);
+                ok = mbar_wait_bounded(bar(B_FULL(s)), (uint32_t)(j / C::kStages) & 1u, abort_flag, status);
                 if (!ok) break;
-                umma_commit(bar(B_EMPTY(slot_of(2 * j + 1))));
+                // Next scores first: S(j+1) may overwrite S once both tiles have read S(j).
+                if (j + 1 < n_max) {
+                    ok = mbar_wait_bounded(bar(B_SFREE), (uint32_t)j & 1u, abort_flag, status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (j + 1 < nA) issue_s(0, ring_k_lo + stage_off);
+                    if (j + 1 < nB) issue_s(1, ring_k_lo + stage_off);
+                    umma_commit(bar(B_SFULL));
+                }
+                ok = mbar_wait_bounded(bar(B_PFULL(j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, status);
+                if (!ok) break;
+                tc_fence_after();
+                if (j < nA) issue_pv(0, j, ring_v_lo + stage_off);
+                if (j < nB) issue_pv(1, j, ring_v_lo + stage_off);
+                umma_commit(bar(B_EMPTY(s)));
             }
             // Tensor memory may be freed only after every issued MMA completed.
             umma_commit(bar(B_MMAFIN));
@@ -360,55 +363,63 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const float sl2 = args.scale_log2;
         float m = -INFINITY;  // running (possibly stale) max of scale*log2(e)*s
         float l = 0.f;        // running sum of 2^(scale*log2(e)*s - m)
-        int reads[2] = {0, 0};  // MMA groups issued so far that read P_X[0] / P_X[1]
+        int reads0 = 0, reads1 = 0;  // MMA groups issued so far that read P_X[0] / P_X[1]
         // Wait until every MMA group that read P_X[b] so far has completed.
         auto wait_p_free = [&](int b) -> bool {
-            if (reads[b] == 0) return true;
-            return __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_PREAD(x, b)), (uint32_t)(reads[b] - 1) & 1u,
-                                                              abort_flag, status));
+            const int r = b ? reads1 : reads0;
+            if (r == 0) return true;
+            return __all_sync(0xffffffffu,
+                              mbar_wait_bounded(bar(B_PREAD(x, b)), (uint32_t)(r - 1) & 1u, abort_flag, status));
         };
         bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_SFULL(x)), (uint32_t)j & 1u, abort_flag, status));
+        // Every step of the CTA, also those past this tile's last one: the shared
+        // handshake barriers need both tiles' arrivals.
+        for (int j = 0; j < n_max; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_SFULL), (uint32_t)j & 1u, abort_flag, status));
             if (!ok) break;
-            tc_fence_after();
+            const bool active = j < n_tiles;
             uint32_t sr[64];
-            tmem_ld_32x32b_x32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tmem_ld_32x32b_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(bar(B_SFREE(x)));  // S_X may now be overwritten by S_X(j+1)
-            const bool masked = fwd_tile_needs_mask(j, qx, Nq, Nk, causal);
-            float alpha;
-            bool rescale;
-            uint32_t ph[32], pl[32];
-            // Two instances of the same step, so the unmasked (common) step carries
-            // no predicated mask or remainder instructions.
-            if (masked)
-                rescale = softmax_step<true, BF16>(sr, j * kFwdBc, lim, sl2, m, l, alpha, ph, pl);
-            else
-                rescale = softmax_step<false, BF16>(sr, 0, 0, sl2, m, l, alpha, ph, pl);
-            const int b = j & 1;
-            // P_X[b] (and on masked steps P_X[b^1]) must no longer be read by an earlier
-            // MMA group; a rescale of O_X needs every earlier group complete (the latest
-            // one read P_X[b^1]).
-            ok = wait_p_free(b) && ((!masked && !(rescale && j > 0)) || wait_p_free(b ^ 1));
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t p_addr = lane_base + C::tmem_p(x, b);
-            tmem_st_32x32b_x16(p_addr, *reinterpret_cast<uint32_t(*)[16]>(&ph[0]));
-            tmem_st_32x32b_x16(p_addr + 16, *reinterpret_cast<uint32_t(*)[16]>(&ph[16]));
-            if (masked) {
-                const uint32_t plo_addr = lane_base + C::tmem_p(x, b ^ 1);
-                tmem_st_32x32b_x16(plo_addr, *reinterpret_cast<uint32_t(*)[16]>(&pl[0]));
-                tmem_st_32x32b_x16(plo_addr + 16, *reinterpret_cast<uint32_t(*)[16]>(&pl[16]));
+            if (active) {
+                tc_fence_after();
+                tmem_ld_32x32b_x32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                tmem_ld_32x32b_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                tmem_wait_ld();
+                tc_fence_before();
             }
-            if (rescale && j > 0) rescale_o<D>(o_addr, alpha);  // O_X holds PV_X(0..j-1), all complete
-            reads[b] += 1;
-            if (masked) reads[b ^ 1] += 1;
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(B_PFULL(x, b)));
+            mbar_arrive(bar(B_SFREE));  // S may now be overwritten by S(j+1)
+            if (active) {
+                const bool masked = fwd_tile_needs_mask(j, qx, Nq, Nk, causal);
+                float alpha;
+                bool rescale;
+                uint32_t ph[32], pl[32];
+                // Two instances of the same step, so the unmasked (common) step carries
+                // no predicated mask or remainder instructions.
+                if (masked)
+                    rescale = softmax_step<true, BF16>(sr, j * kFwdBc, lim, sl2, m, l, alpha, ph, pl);
+                else
+                    rescale = softmax_step<false, BF16>(sr, 0, 0, sl2, m, l, alpha, ph, pl);
+                const int b = j & 1;
+                // P_X[b] (and on masked steps P_X[b^1]) must no longer be read by an earlier
+                // MMA group; a rescale of O_X needs every earlier group complete (the latest
+                // one read P_X[b^1]).
+                ok = wait_p_free(b) && ((!masked && !(rescale && j > 0)) || wait_p_free(b ^ 1));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t p_addr = lane_base + C::tmem_p(x, b);
+                tmem_st_32x32b_x16(p_addr, *reinterpret_cast<uint32_t(*)[16]>(&ph[0]));
+                tmem_st_32x32b_x16(p_addr + 16, *reinterpret_cast<uint32_t(*)[16]>(&ph[16]));
+                if (masked) {
+                    const uint32_t plo_addr = lane_base + C::tmem_p(x, b ^ 1);
+                    tmem_st_32x32b_x16(plo_addr, *reinterpret_cast<uint32_t(*)[16]>(&pl[0]));
+                    tmem_st_32x32b_x16(plo_addr + 16, *reinterpret_cast<uint32_t(*)[16]>(&pl[16]));
+                }
+                if (rescale && j > 0) rescale_o<D>(o_addr, alpha);  // O_X holds PV_X(0..j-1), all complete
+                reads0 += (b == 0 || masked) ? 1 : 0;
+                reads1 += (b == 1 || masked) ? 1 : 0;
+                tmem_wait_st();
+                tc_fence_before();
+            }
+            mbar_arrive(bar(B_PFULL(j & 1)));
         }
         if (ok && n_tiles > 0) {
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_OFINAL(x)), 0, abort_flag, status));
