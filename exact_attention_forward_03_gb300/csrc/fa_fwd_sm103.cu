@@ -11,35 +11,33 @@
 // element-wise only on tiles that straddle it or the ragged Nk tail (§5.3;
 // "02 · FA2", §4).
 //
-// Roles (warp specialisation, 10 warps):
-//   warps 0-3  softmax of Q tile A, one thread per query row (TMEM lane = row)
-//   warps 4-7  softmax of Q tile B
-//   warp 8     TMA producer: both Q tiles and K_0 once, then one ring stage per
-//              step j holding V_j and K_{j+1} (64 keys each)
-//   warp 9     owns tensor memory; one lane issues every tcgen05.mma
+// Roles (warp specialisation, three warpgroups):
+//   warps 0-3   softmax of Q tile A: one thread per query row (TMEM lane = row),
+//               the whole 128-key row of S in registers
+//   warps 4-7   the same for Q tile B
+//   warp 8      TMA producer: both Q tiles once, then K_0, V_0, K_1, V_1, ...
+//               through a ring of shared-memory slots (full/empty mbarriers)
+//   warp 9      owns tensor memory; one lane issues every tcgen05.mma
+//   warps 10-11 idle (they complete the third warpgroup for the register split)
+// The launch gives 168 registers per thread; the third warpgroup drops to 104
+// and the softmax warpgroups rise to 200 (2 * 200 + 104 = 3 * 168).
 //
-// Tensor memory (512 columns), for each tile X: S_X (64 fp32 columns), two P
-// buffers P_X[0], P_X[1] (64 keys as 16-bit pairs, 32 columns each) and O_X (d
-// fp32 columns).  Because P has its own columns, S_X(j+1) = Q_X K_{j+1}^T is
-// issued as soon as the softmax warps have read S_X(j) into registers, before
-// O_X += P_X(j) V_j: the tensor core computes the next scores while the
-// softmax of the current step runs, and the two tiles keep it fed.  Step j
-// writes P_X[j % 2], so the softmax of step j waits only for the MMA that read
-// that buffer two steps earlier.  MMA order per step j: S_A(j+1), S_B(j+1),
-// PV_A(j), PV_B(j).
+// Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A [256,384),
+// O_B [384,512).  Once a softmax thread holds its row of S_X in registers it
+// writes P_X as 16-bit pairs over the first 64 columns of S_X (and, on steps
+// that need a mask, the 16-bit remainder P - P_head over the next 64: rows near
+// the diagonal see few keys, so one 16-bit rounding of their few large weights
+// would otherwise dominate their error; both parts are multiplied into O).
 //
-// On steps that need a mask, P is written as a 16-bit head P plus a 16-bit
-// remainder P - P_head in the other buffer, and both are multiplied into O:
-// rows near the diagonal see few keys, so one 16-bit rounding of their few
-// large weights would otherwise dominate their error.  Every MMA group that
-// reads a P buffer commits to that buffer's barrier, and both sides count those
-// uses the same way, so the softmax always knows which phase to wait for.
-//
-// The two tiles share the barriers of the per-step handshakes (S ready, S read,
-// P ready): the MMA warp waits once per step for both tiles, which keeps its
-// serial bookkeeping between MMA groups short.  A tile with fewer steps than
-// its partner keeps arriving on those barriers, paced by "S ready", until the
-// partner is done.
+// The two Q tiles ping-pong on the tensor core.  MMA issue order per K/V step j:
+//   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+// so while the softmax warps of one tile turn S into P, the tensor core runs the
+// other tile's O += P V and next S.  tcgen05.mma operations of one thread run in
+// issue order, so S_X(j+1) overwrites S_X only after PV_X(j) has read P_X(j);
+// and the commit that signals S_X(j+1) also covers PV_X(j), so the softmax may
+// rescale O_X as soon as S_X(j+1) is ready.  Each tile's softmax is on the
+// critical path once per step, so its row is handled by one thread (no
+// cross-warp exchange) and each warp signals "P ready" with one arrival.
 //
 // The rescale of O by alpha = 2^(m_old - m_new) is done only when the row max
 // of some row in the warp grew by more than 2^8: otherwise m stays and p may
@@ -54,8 +52,10 @@
 
 namespace fa {
 
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 384;
 constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr uint32_t kRegsSoftmax = 200;
+constexpr uint32_t kRegsOther = 104;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
@@ -66,31 +66,28 @@ struct FwdCfg {
     static constexpr int kKVBlockBytes = kFwdBc * 128;   // one 64-column block of a K/V tile
     static constexpr int kQBytes = kFwdBr * D * 2;       // one Q tile
     static constexpr int kTileBytes = kFwdBc * D * 2;    // one K or V tile
-    static constexpr int kStages = (D == 128) ? 4 : 8;  // ring stages of (V_j, K_{j+1})
-    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kStages = (D == 128) ? 4 : 8;   // ring slots (K and V alternate)
     static constexpr int kOffQ = 0;                      // Q_A, then Q_B
-    static constexpr int kOffK0 = kFwdTilesPerCta * kQBytes;
-    static constexpr int kOffRing = kOffK0 + kTileBytes;
-    static constexpr int kOffBar = kOffRing + kStages * kStageBytes;
-    // barriers: q_full, full[S], empty[S], s_full, s_free, p_full[2], p_read[2][2], o_final[2], mma_fin
-    static constexpr int kNumBars = 1 + 2 * kStages + 1 + 1 + 2 + 4 + 2 + 1;
+    static constexpr int kOffRing = kFwdTilesPerCta * kQBytes;
+    static constexpr int kOffBar = kOffRing + kStages * kTileBytes;
+    // barriers: q_full, full[S], empty[S], s_full[2], p_full[2], o_final[2], mma_fin
+    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
     static constexpr uint32_t kTmemCols = 512;
-    __device__ static constexpr uint32_t tmem_s(int x) { return 64u * x; }          // [0,64), [64,128)
-    __device__ static constexpr uint32_t tmem_p(int x, int b) { return 128u + 64u * x + 32u * b; }  // [128,256)
-    __device__ static constexpr uint32_t tmem_o(int x) { return 256u + (uint32_t)D * x; }
+    __device__ static constexpr uint32_t tmem_s(int x) { return 128u * x; }
+    __device__ static constexpr uint32_t tmem_o(int x) { return 256u + 128u * x; }
 };
 
-// Step j needs element masks when it crosses the ragged end of K or, under
+// K/V tile j needs element masks when it crosses the ragged end of K or, under
 // causal masking, holds a key beyond the first row's last visible key.
 __device__ __forceinline__ bool fwd_tile_needs_mask(int j, int q0, int Nq, int Nk, int causal) {
     const int last_key = (j + 1) * kFwdBc - 1;
     return (last_key >= Nk) || (causal && last_key > q0 + (Nk - Nq));
 }
 
-// K/V steps that Q rows [q0, q0+128) must visit (0 when the tile holds no row).
+// K/V tiles that Q rows [q0, q0+128) must visit (0 when the tile holds no row).
 __device__ __forceinline__ int fwd_tile_count(int q0, int Nq, int Nk, int causal) {
     if (q0 >= Nq) return 0;
     int kv_end = Nk;
@@ -98,9 +95,87 @@ __device__ __forceinline__ int fwd_tile_count(int q0, int Nq, int Nk, int causal
     return kv_end > 0 ? (kv_end + kFwdBc - 1) / kFwdBc : 0;
 }
 
+// State of one softmax thread's row after a step.
+struct RowStep {
+    float m;       // running (possibly stale) max of scale*log2(e)*s
+    float l;       // running sum of 2^(scale*log2(e)*s - m)
+    float alpha;   // factor O is to be scaled by in this step
+    bool rescale;  // whether the warp moved its max in this step
+};
+
+// One online-softmax step of this thread's row over one K/V tile: S (128 fp32
+// columns of TMEM at s_addr) into registers, optional causal/tail mask,
+// (conditional) max update, p = 2^(s*c - m), the row sum, and P written back
+// as 16-bit pairs over the first 64 columns (the 16-bit remainder over the
+// next 64 on masked tiles).  Keys [16k, 16k+16) land in columns [8k, 8k+8).
+template <bool MASKED, bool BF16>
+__device__ __forceinline__ RowStep softmax_tile(uint32_t s_addr, int c0, int lim, float sl2, float m, float l) {
+    using PK = Pack<BF16>;
+    uint32_t s[128];
+    tmem_ld_32x32b_x32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+    tmem_ld_32x32b_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+    tmem_ld_32x32b_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+    tmem_ld_32x32b_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+    tmem_wait_ld();
+    if (MASKED) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+            if (c0 + c > lim) s[c] = __float_as_uint(-INFINITY);
+    }
+    float mx[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mx[e] = fmax3(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), -INFINITY);
+#pragma unroll
+    for (int c = 16; c < 128; c += 2)
+        mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+    const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+    const float m_cand = fmaxf(m, mt * sl2);
+    RowStep r;
+    r.rescale = __any_sync(0xffffffffu, m_cand > m + kRescaleThreshold);
+    r.alpha = 1.f;
+    if (r.rescale) {
+        const float m_new_d = (m_cand == -INFINITY) ? 0.f : m_cand;  // never subtract -inf from -inf
+        r.alpha = ex2_approx(m - m_new_d);
+        m = m_cand;
+    }
+    r.m = m;
+    const float m_d = (m == -INFINITY) ? 0.f : m;
+    const uint64_t scale2 = f2_make(sl2, sl2);
+    const uint64_t shift2 = f2_make(-m_d, -m_d);
+    uint64_t rs2[4] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f), f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t ph[16], pl[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            const int col = 32 * c + e;
+            const float2 xa = f2_split(ffma2(f2_make(__uint_as_float(s[col]), __uint_as_float(s[col + 1])), scale2, shift2));
+            const float p0 = ex2_approx(xa.x);
+            const float p1 = ex2_approx(xa.y);
+            rs2[(e >> 1) & 3] = fadd2(rs2[(e >> 1) & 3], f2_make(p0, p1));
+            ph[e >> 1] = PK::pack(p0, p1);
+            if (MASKED) {
+                const float2 hf = PK::unpack(ph[e >> 1]);
+                pl[e >> 1] = PK::pack(p0 - hf.x, p1 - hf.y);
+            }
+        }
+        tmem_st_32x32b_x16(s_addr + 16 * c, ph);
+        if (MASKED) tmem_st_32x32b_x16(s_addr + 64 + 16 * c, pl);
+    }
+    const float2 r0 = f2_split(fadd2(rs2[0], rs2[1])), r1 = f2_split(fadd2(rs2[2], rs2[3]));
+    r.l = l * r.alpha + ((r0.x + r0.y) + (r1.x + r1.y));
+    return r;
+}
+
+// The masked step is taken about once per Q tile, so it is kept out of line to
+// leave the registers and code of the common step alone.
+template <bool BF16>
+__device__ __noinline__ RowStep softmax_tile_masked(uint32_t s_addr, int c0, int lim, float sl2, float m, float l) {
+    return softmax_tile<true, BF16>(s_addr, c0, lim, sl2, m, l);
+}
+
 // O_X (32 rows of this warp, kCols columns) *= alpha, 16 columns at a time.
-// Rarely taken (only when a row max grows by more than 2^8), so it is kept out
-// of line to leave the registers of the common path alone.
+// Rarely taken (only when a row max grows by more than 2^8).
 template <int kCols>
 __device__ __noinline__ void rescale_o(uint32_t o_addr, float alpha) {
     const uint64_t a2 = f2_make(alpha, alpha);
@@ -117,56 +192,6 @@ __device__ __noinline__ void rescale_o(uint32_t o_addr, float alpha) {
         }
         tmem_st_32x32b_x16(o_addr + 16 * c, orow);
     }
-}
-
-// One online-softmax step for the 64 S values of this thread's row held in
-// `sr` (fp32 bits): optional causal/tail mask, (conditional) max update,
-// p = 2^(s*c - m), the row sum, and P packed into 16-bit pairs in `ph` (plus
-// the 16-bit remainder in `pl` on masked tiles).  Returns whether the warp
-// moved its max; `alpha` is then the factor O and l are scaled by.
-template <bool MASKED, bool BF16>
-__device__ __forceinline__ bool softmax_step(uint32_t (&sr)[64], int c0, int lim, float sl2, float &m, float &l,
-                                             float &alpha, uint32_t (&ph)[32], uint32_t (&pl)[32]) {
-    using PK = Pack<BF16>;
-    if (MASKED) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-            if (c0 + c > lim) sr[c] = __float_as_uint(-INFINITY);
-    }
-    float mx[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) mx[e] = fmax3(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]), -INFINITY);
-#pragma unroll
-    for (int c = 16; c < 64; c += 2)
-        mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-    const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-    const float m_cand = fmaxf(m, mt * sl2);
-    const bool rescale = __any_sync(0xffffffffu, m_cand > m + kRescaleThreshold);
-    alpha = 1.f;
-    if (rescale) {
-        const float m_new_d = (m_cand == -INFINITY) ? 0.f : m_cand;  // never subtract -inf from -inf
-        alpha = ex2_approx(m - m_new_d);
-        m = m_cand;
-    }
-    const float m_d = (m == -INFINITY) ? 0.f : m;
-    const uint64_t scale2 = f2_make(sl2, sl2);
-    const uint64_t shift2 = f2_make(-m_d, -m_d);
-    uint64_t rs2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
-#pragma unroll
-    for (int e = 0; e < 64; e += 2) {
-        const float2 xa = f2_split(ffma2(f2_make(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), scale2, shift2));
-        const float p0 = ex2_approx(xa.x);
-        const float p1 = ex2_approx(xa.y);
-        rs2[(e >> 1) & 1] = fadd2(rs2[(e >> 1) & 1], f2_make(p0, p1));
-        ph[e >> 1] = PK::pack(p0, p1);
-        if (MASKED) {
-            const float2 hf = PK::unpack(ph[e >> 1]);
-            pl[e >> 1] = PK::pack(p0 - hf.x, p1 - hf.y);
-        }
-    }
-    const float2 r0 = f2_split(rs2[0]), r1 = f2_split(rs2[1]);
-    l = l * alpha + ((r0.x + r0.y) + (r1.x + r1.y));
-    return rescale;
 }
 
 template <int D, bool BF16>
@@ -196,14 +221,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     constexpr int B_QFULL = 0;
     auto B_FULL = [](int s) { return 1 + s; };
     auto B_EMPTY = [](int s) { return 1 + C::kStages + s; };
-    constexpr int B_SFULL = 1 + 2 * C::kStages;  // S_A(j), S_B(j) ready
-    constexpr int B_SFREE = 2 + 2 * C::kStages;  // both tiles have read S(j)
-    // P[b] written by both tiles: one barrier per buffer, so the softmax (which may
-    // run a step ahead of the MMA warp) can never complete a phase twice unseen.
-    auto B_PFULL = [](int b) { return 3 + 2 * C::kStages + b; };
-    auto B_PREAD = [](int x, int b) { return 5 + 2 * C::kStages + 2 * x + b; };  // an MMA group read P_X[b]
-    auto B_OFINAL = [](int x) { return 9 + 2 * C::kStages + x; };
-    constexpr int B_MMAFIN = 11 + 2 * C::kStages;
+    auto B_SFULL = [](int x) { return 1 + 2 * C::kStages + x; };   // S_X(j) in TMEM
+    auto B_PFULL = [](int x) { return 3 + 2 * C::kStages + x; };   // P_X(j) in TMEM (one arrival per warp)
+    auto B_OFINAL = [](int x) { return 5 + 2 * C::kStages + x; };  // last PV_X complete
+    constexpr int B_MMAFIN = 7 + 2 * C::kStages;
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
     int *status = args.status;
@@ -214,13 +235,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_init(bar(B_FULL(s)), 1);
             mbar_init(bar(B_EMPTY(s)), 1);
         }
-        mbar_init(bar(B_SFULL), 1);
-        mbar_init(bar(B_SFREE), 256);
-        mbar_init(bar(B_PFULL(0)), 256);
-        mbar_init(bar(B_PFULL(1)), 256);
         for (int x = 0; x < 2; ++x) {
-            mbar_init(bar(B_PREAD(x, 0)), 1);
-            mbar_init(bar(B_PREAD(x, 1)), 1);
+            mbar_init(bar(B_SFULL(x)), 1);
+            mbar_init(bar(B_PFULL(x)), 4);
             mbar_init(bar(B_OFINAL(x)), 1);
         }
         mbar_init(bar(B_MMAFIN), 1);
@@ -240,31 +257,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == kWarpTma) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0 && n_max > 0) {
+    if (warp >= 8) {
+        regs_decrease<kRegsOther>();
+        if (warp == kWarpTma && lane == 0 && n_max > 0) {
+            // ------------------------------------------------------------ TMA producer
             uint32_t pend_mask = 0, pend_par = 0;
-            mbar_arrive_expect_tx(bar(B_QFULL), kFwdTilesPerCta * C::kQBytes + C::kTileBytes);
+            mbar_arrive_expect_tx(bar(B_QFULL), kFwdTilesPerCta * C::kQBytes);
             for (int x = 0; x < kFwdTilesPerCta; ++x)
                 for (int b = 0; b < C::kBlocks; ++b)
                     tma_load_3d(sb + C::kOffQ + x * C::kQBytes + b * C::kQBlockBytes, &tmQ, b * 64,
                                 q0 + x * kFwdBr, bh, bar(B_QFULL));
-            for (int b = 0; b < C::kBlocks; ++b)
-                tma_load_3d(sb + C::kOffK0 + b * C::kKVBlockBytes, &tmK, b * 64, 0, bh, bar(B_QFULL));
-            for (int j = 0; j < n_max; ++j) {
-                // stage j % kStages: V_j, then K_{j+1} (absent on the last step)
-                const int s = j % C::kStages;
-                const uint32_t it = (uint32_t)(j / C::kStages);
+            // Slot t holds K_{t/2} (t even) or V_{t/2} (t odd).
+            for (int t = 0; t < 2 * n_max; ++t) {
+                const int s = t % C::kStages;
+                const uint32_t it = (uint32_t)(t / C::kStages);
                 if (!mbar_wait_bounded(bar(B_EMPTY(s)), (it & 1u) ^ 1u, abort_flag, status)) break;
-                const bool next = j + 1 < n_max;
-                mbar_arrive_expect_tx(bar(B_FULL(s)), next ? 2 * C::kTileBytes : C::kTileBytes);
-                const uint32_t dst = sb + C::kOffRing + s * C::kStageBytes;
+                mbar_arrive_expect_tx(bar(B_FULL(s)), C::kTileBytes);
+                const CUtensorMap *map = (t & 1) ? &tmV : &tmK;
+                const uint32_t dst = sb + C::kOffRing + s * C::kTileBytes;
                 for (int b = 0; b < C::kBlocks; ++b)
-                    tma_load_3d(dst + b * C::kKVBlockBytes, &tmV, b * 64, j * kFwdBc, bh, bar(B_FULL(s)));
-                if (next)
-                    for (int b = 0; b < C::kBlocks; ++b)
-                        tma_load_3d(dst + C::kTileBytes + b * C::kKVBlockBytes, &tmK, b * 64, (j + 1) * kFwdBc, bh,
-                                    bar(B_FULL(s)));
+                    tma_load_3d(dst + b * C::kKVBlockBytes, map, b * 64, (t >> 1) * kFwdBc, bh, bar(B_FULL(s)));
                 pend_mask |= 1u << s;
                 pend_par = (pend_par & ~(1u << s)) | ((it & 1u) << s);
             }
@@ -273,76 +285,84 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_wait_bounded(bar(B_QFULL), 0, &no_abort, status);
             for (int s = 0; s < C::kStages; ++s)
                 if (pend_mask & (1u << s)) mbar_wait_bounded(bar(B_FULL(s)), (pend_par >> s) & 1u, &no_abort, status);
-        }
-    } else if (warp == kWarpMma) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n_max > 0) {
+        } else if (warp == kWarpMma && lane == 0 && n_max > 0) {
+            // ------------------------------------------------------------ MMA issuer
             constexpr uint32_t idesc_qk = idesc_f16(128, kFwdBc, BF16, false);
             constexpr uint32_t idesc_pv = idesc_f16(128, D, BF16, true);
             // Descriptors are built once; per instruction only the address field of the
-            // low word moves (by a compile-time offset plus the stage offset).
+            // low word moves (by a compile-time offset plus the slot offset).
             constexpr uint32_t hi = sdesc_hi_sw128(1024);                        // 8 rows x 128 B per core group
             const uint32_t q_lo = sdesc_lo(sb + C::kOffQ, 16);                   // K-major: LBO unused
-            const uint32_t k0_lo = sdesc_lo(sb + C::kOffK0, 16);
-            const uint32_t ring_k_lo = sdesc_lo(sb + C::kOffRing + C::kTileBytes, 16);
-            const uint32_t ring_v_lo = sdesc_lo(sb + C::kOffRing, C::kKVBlockBytes);  // MN-major: LBO = 64-col block
-            // S_X = Q_X K^T for the K tile whose descriptor low word is k_lo: K-major A and
-            // B, N = 64 keys, 16 of the d columns per instruction.
-            auto issue_s = [&](int x, uint32_t k_lo) {
+            const uint32_t k_lo = sdesc_lo(sb + C::kOffRing, 16);
+            const uint32_t v_lo = sdesc_lo(sb + C::kOffRing, C::kKVBlockBytes);  // MN-major: LBO = 64-col block
+            auto slot_off = [](int t) { return (uint32_t)((t % C::kStages) * (C::kTileBytes >> 4)); };
+            auto wait_slot = [&](int t) {
+                return mbar_wait_bounded(bar(B_FULL(t % C::kStages)), (uint32_t)(t / C::kStages) & 1u, abort_flag,
+                                         status);
+            };
+            // S_X = Q_X K^T for the K tile in slot t: K-major A and B, 16 of the d
+            // columns per instruction; its commit also covers every earlier MMA.
+            auto issue_s = [&](int x, int t) {
                 const uint32_t qx_lo = q_lo + x * (C::kQBytes >> 4);
+                const uint32_t kt_lo = k_lo + slot_off(t);
                 const uint32_t d_s = tmem + C::tmem_s(x);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off_q = ((k >> 2) * C::kQBlockBytes + (k & 3) * 32) >> 4;
                     const uint32_t off_k = ((k >> 2) * C::kKVBlockBytes + (k & 3) * 32) >> 4;
-                    umma_ss_w(d_s, qx_lo + off_q, hi, k_lo + off_k, hi, idesc_qk, k > 0 ? 1u : 0u);
+                    umma_ss_w(d_s, qx_lo + off_q, hi, kt_lo + off_k, hi, idesc_qk, k > 0 ? 1u : 0u);
                 }
+                umma_commit(bar(B_SFULL(x)));
             };
-            // O_X += P_X(j) V_j: P from TMEM buffer j % 2 (the remainder, on masked steps,
-            // from the other buffer), V as an MN-major operand, 16 keys per instruction.
-            auto issue_pv = [&](int x, int j, uint32_t vj_lo) {
+            // O_X += P_X(j) V_j: P from TMEM (the remainder too on masked tiles), V as an
+            // MN-major operand, 16 keys per instruction.
+            auto issue_pv = [&](int x, int j, int t) {
+                const uint32_t vt_lo = v_lo + slot_off(t);
                 const uint32_t d_o = tmem + C::tmem_o(x);
-                const int b = j & 1;
+                const uint32_t p_t = tmem + C::tmem_s(x);
 #pragma unroll
                 for (int k = 0; k < kFwdBc / 16; ++k)
-                    umma_ts_w(d_o, tmem + C::tmem_p(x, b) + 8 * k, vj_lo + ((k * 2048) >> 4), hi, idesc_pv,
-                              (j > 0 || k > 0) ? 1u : 0u);
-                umma_commit(bar(B_PREAD(x, b)));
+                    umma_ts_w(d_o, p_t + 8 * k, vt_lo + ((k * 2048) >> 4), hi, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
                 if (fwd_tile_needs_mask(j, q0 + x * kFwdBr, Nq, Nk, causal)) {
 #pragma unroll
                     for (int k = 0; k < kFwdBc / 16; ++k)
-                        umma_ts_w(d_o, tmem + C::tmem_p(x, b ^ 1) + 8 * k, vj_lo + ((k * 2048) >> 4), hi, idesc_pv, 1u);
-                    umma_commit(bar(B_PREAD(x, b ^ 1)));
+                        umma_ts_w(d_o, p_t + 64 + 8 * k, vt_lo + ((k * 2048) >> 4), hi, idesc_pv, 1u);
                 }
-                if (j == (x == 0 ? nA : nB) - 1) umma_commit(bar(B_OFINAL(x)));
             };
-            bool ok = mbar_wait_bounded(bar(B_QFULL), 0, abort_flag, status);
+            bool ok = mbar_wait_bounded(bar(B_QFULL), 0, abort_flag, status) && wait_slot(0);
             if (ok) {
                 tc_fence_after();
-                if (nA > 0) issue_s(0, k0_lo);
-                if (nB > 0) issue_s(1, k0_lo);
-                umma_commit(bar(B_SFULL));
+                if (nA > 0) issue_s(0, 0);
+                if (nB > 0) issue_s(1, 0);
+                umma_commit(bar(B_EMPTY(0)));
             }
             for (int j = 0; ok && j < n_max; ++j) {
-                const int s = j % C::kStages;
-                const uint32_t stage_off = s * (C::kStageBytes >> 4);
-                ok = mbar_wait_bounded(bar(B_FULL(s)), (uint32_t)(j / C::kStages) & 1u, abort_flag, status);
-                if (!ok) break;
-                // Next scores first: S(j+1) may overwrite S once both tiles have read S(j).
-                if (j + 1 < n_max) {
-                    ok = mbar_wait_bounded(bar(B_SFREE), (uint32_t)j & 1u, abort_flag, status);
+                const int tv = 2 * j + 1, tk = 2 * j + 2;  // slots of V_j and K_{j+1}
+                bool v_ready = false, k_ready = false;
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    const int nx = x == 0 ? nA : nB;
+                    if (j >= nx) continue;
+                    // P_X(j) first: it is the wait most likely to block.
+                    ok = mbar_wait_bounded(bar(B_PFULL(x)), (uint32_t)j & 1u, abort_flag, status);
+                    if (ok && !v_ready) ok = v_ready = wait_slot(tv);
                     if (!ok) break;
                     tc_fence_after();
-                    if (j + 1 < nA) issue_s(0, ring_k_lo + stage_off);
-                    if (j + 1 < nB) issue_s(1, ring_k_lo + stage_off);
-                    umma_commit(bar(B_SFULL));
+                    issue_pv(x, j, tv);
+                    if (j + 1 < nx) {
+                        if (!k_ready) {
+                            ok = k_ready = wait_slot(tk);
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        issue_s(x, tk);
+                    } else {
+                        umma_commit(bar(B_OFINAL(x)));
+                    }
                 }
-                ok = mbar_wait_bounded(bar(B_PFULL(j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, status);
                 if (!ok) break;
-                tc_fence_after();
-                if (j < nA) issue_pv(0, j, ring_v_lo + stage_off);
-                if (j < nB) issue_pv(1, j, ring_v_lo + stage_off);
-                umma_commit(bar(B_EMPTY(s)));
+                umma_commit(bar(B_EMPTY(tv % C::kStages)));
+                if (j + 1 < n_max) umma_commit(bar(B_EMPTY(tk % C::kStages)));
             }
             // Tensor memory may be freed only after every issued MMA completed.
             umma_commit(bar(B_MMAFIN));
@@ -351,6 +371,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax / correction / epilogue
+        regs_increase<kRegsSoftmax>();
         const int x = warp >> 2;       // Q tile of this warp
         const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter+32) belong to this warp
         const int qx = q0 + x * kFwdBr;
@@ -363,63 +384,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const float sl2 = args.scale_log2;
         float m = -INFINITY;  // running (possibly stale) max of scale*log2(e)*s
         float l = 0.f;        // running sum of 2^(scale*log2(e)*s - m)
-        int reads0 = 0, reads1 = 0;  // MMA groups issued so far that read P_X[0] / P_X[1]
-        // Wait until every MMA group that read P_X[b] so far has completed.
-        auto wait_p_free = [&](int b) -> bool {
-            const int r = b ? reads1 : reads0;
-            if (r == 0) return true;
-            return __all_sync(0xffffffffu,
-                              mbar_wait_bounded(bar(B_PREAD(x, b)), (uint32_t)(r - 1) & 1u, abort_flag, status));
-        };
         bool ok = true;
-        // Every step of the CTA, also those past this tile's last one: the shared
-        // handshake barriers need both tiles' arrivals.
-        for (int j = 0; j < n_max; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_SFULL), (uint32_t)j & 1u, abort_flag, status));
+        for (int j = 0; j < n_tiles; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_SFULL(x)), (uint32_t)j & 1u, abort_flag, status));
             if (!ok) break;
-            const bool active = j < n_tiles;
-            uint32_t sr[64];
-            if (active) {
-                tc_fence_after();
-                tmem_ld_32x32b_x32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-                tmem_ld_32x32b_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-                tmem_wait_ld();
-                tc_fence_before();
-            }
-            mbar_arrive(bar(B_SFREE));  // S may now be overwritten by S(j+1)
-            if (active) {
-                const bool masked = fwd_tile_needs_mask(j, qx, Nq, Nk, causal);
-                float alpha;
-                bool rescale;
-                uint32_t ph[32], pl[32];
-                // Two instances of the same step, so the unmasked (common) step carries
-                // no predicated mask or remainder instructions.
-                if (masked)
-                    rescale = softmax_step<true, BF16>(sr, j * kFwdBc, lim, sl2, m, l, alpha, ph, pl);
-                else
-                    rescale = softmax_step<false, BF16>(sr, 0, 0, sl2, m, l, alpha, ph, pl);
-                const int b = j & 1;
-                // P_X[b] (and on masked steps P_X[b^1]) must no longer be read by an earlier
-                // MMA group; a rescale of O_X needs every earlier group complete (the latest
-                // one read P_X[b^1]).
-                ok = wait_p_free(b) && ((!masked && !(rescale && j > 0)) || wait_p_free(b ^ 1));
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t p_addr = lane_base + C::tmem_p(x, b);
-                tmem_st_32x32b_x16(p_addr, *reinterpret_cast<uint32_t(*)[16]>(&ph[0]));
-                tmem_st_32x32b_x16(p_addr + 16, *reinterpret_cast<uint32_t(*)[16]>(&ph[16]));
-                if (masked) {
-                    const uint32_t plo_addr = lane_base + C::tmem_p(x, b ^ 1);
-                    tmem_st_32x32b_x16(plo_addr, *reinterpret_cast<uint32_t(*)[16]>(&pl[0]));
-                    tmem_st_32x32b_x16(plo_addr + 16, *reinterpret_cast<uint32_t(*)[16]>(&pl[16]));
-                }
-                if (rescale && j > 0) rescale_o<D>(o_addr, alpha);  // O_X holds PV_X(0..j-1), all complete
-                reads0 += (b == 0 || masked) ? 1 : 0;
-                reads1 += (b == 1 || masked) ? 1 : 0;
-                tmem_wait_st();
-                tc_fence_before();
-            }
-            mbar_arrive(bar(B_PFULL(j & 1)));
+            tc_fence_after();
+            // Two instances of the same step, so the unmasked (common) tile carries no
+            // predicated mask or remainder instructions.
+            const RowStep r = fwd_tile_needs_mask(j, qx, Nq, Nk, causal)
+                                  ? softmax_tile_masked<BF16>(s_addr, j * kFwdBc, lim, sl2, m, l)
+                                  : softmax_tile<false, BF16>(s_addr, 0, 0, sl2, m, l);
+            m = r.m;
+            l = r.l;
+            if (r.rescale && j > 0) rescale_o<D>(o_addr, r.alpha);  // O_X holds PV_X(0..j-1), all complete
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_PFULL(x)));
         }
         if (ok && n_tiles > 0) {
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_OFINAL(x)), 0, abort_flag, status));
