@@ -18,6 +18,7 @@ Under torchrun every rank runs an independent replica; rank 0 prints.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -400,13 +401,34 @@ def run_fa(args, rank, world, local):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"],
                      "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                     "traffic": args.traffic, "peak_source": peak_src,
+                     "traffic": args.traffic if args.traffic is not None else captured_traffic("fa_fwd_kernel<128,bf16>", w.name),
+                     "peak_source": peak_src,
                      "kernel": "fa_fwd_kernel<128,bf16>", "flops_per_launch": flops},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "decode": decode,
         "wall_s_fwd_timed": wall, "ms_fwd_min": min(ms), "ms_fwd_median": statistics.median(ms),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def captured_traffic(kernel, workload):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from the ncu
+    capture summarised under profiles/, or None when there is none or when the
+    kernel's sources changed since the counters were taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            entry = json.load(f).get(kernel)
+        if entry is None or entry.get("workload") != workload:
+            return None
+        h = hashlib.sha256()
+        for rel in entry["source_files"]:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != entry["source_sha256"]:
+            return None
+        return float(entry["dram_bytes_read"] + entry["dram_bytes_write"])
+    except (OSError, ValueError, KeyError):
+        return None
 
 
 def main(argv=None):
