@@ -1,48 +1,50 @@
 // fa_fwd_sm103.cu -- fused exact attention forward on sm_103a tensor cores.
 //
-// One CTA computes two 128-row Q tiles (A and B, 256 consecutive query rows) of
-// one (batch, head):
+// One CTA computes one 128-row Q tile of one (batch, head):
 //   O_i = sum_j softmax_j(scale * q_i . k_j + mask) v_j,  LSE_i = m_i + ln l_i
 // following the FlashAttention-2 forward ("6.2 FlashAttention V2 explained",
-// §6): the Q tiles stay on chip, K/V tiles stream past them, a running row max
-// m and row sum l are kept per row, the accumulator is rescaled by
+// §6): the Q tile stays on chip, K/V tiles stream past it, a running row max m
+// and row sum l are kept per row, the accumulator is rescaled by
 // exp(m_old - m_new) and divided by l once at the end (§3.2; "02 · FA2", §1).
 // Causal masking visits only K/V tiles up to the diagonal and masks
 // element-wise only on tiles that straddle it or the ragged Nk tail (§5.3;
 // "02 · FA2", §4).
 //
-// Roles (warp specialisation, three warpgroups):
-//   warps 0-3   softmax of Q tile A: one thread per query row (TMEM lane = row),
-//               the whole 128-key row of S in registers
-//   warps 4-7   the same for Q tile B
-//   warp 8      TMA producer: both Q tiles once, then K_0, V_0, K_1, V_1, ...
-//               through a ring of shared-memory slots (full/empty mbarriers)
-//   warp 9      owns tensor memory; one lane issues every tcgen05.mma
-//   warps 10-11 idle (they complete the third warpgroup for the register split)
-// The launch gives 168 registers per thread; the third warpgroup drops to 104
-// and the softmax warpgroups rise to 200 (2 * 200 + 104 = 3 * 168).
+// Roles (warp specialisation, 8 warps):
+//   warps 0-3  softmax: one thread per query row (TMEM lane = row), the whole
+//              128-key row of S in registers
+//   warp 4     TMA producer: the Q tile once, then K_0, K_1, K_2, V_0, K_3,
+//              V_1, K_4, ... into two rings of shared-memory slots, one for K
+//              tiles and one for V tiles (full/empty mbarriers per slot)
+//   warp 5     owns tensor memory; one lane issues O += P(j) V_j for every j
+//   warp 6     one lane issues S(t) = Q K_t^T for every t
+//   warp 7     idle
 //
-// Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A [256,384),
-// O_B [384,512).  Once a softmax thread holds its row of S_X in registers it
-// writes P_X as 16-bit pairs over the first 64 columns of S_X (and, on steps
-// that need a mask, the 16-bit remainder P - P_head over the next 64: rows near
-// the diagonal see few keys, so one 16-bit rounding of their few large weights
-// would otherwise dominate their error; both parts are multiplied into O).
+// Tensor memory (512 columns): three score buffers S[0..2] = [0,128),
+// [128,256), [256,384), and O = [384, 384+d).  Tile j's scores go to
+// S[j % 3].  Once a softmax thread holds its row of S(j) in registers it
+// writes P(j) as 16-bit pairs over the first 64 columns of that buffer (and,
+// on tiles that need a mask, the 16-bit remainder P - P_head over the next 64:
+// rows near the diagonal see few keys, so one 16-bit rounding of their few
+// large weights would otherwise dominate their error; both parts are
+// multiplied into O).
 //
-// The two Q tiles ping-pong on the tensor core.  MMA issue order per K/V step j:
-//   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
-// so while the softmax warps of one tile turn S into P, the tensor core runs the
-// other tile's O += P V and next S.  tcgen05.mma operations of one thread run in
-// issue order, so S_X(j+1) overwrites S_X only after PV_X(j) has read P_X(j);
-// and the commit that signals S_X(j+1) also covers PV_X(j), so the softmax may
-// rescale O_X as soon as S_X(j+1) is ready.  Each tile's softmax is on the
-// critical path once per step, so its row is handled by one thread (no
-// cross-warp exchange) and each warp signals "P ready" with one arrival.
+// S(t) may overwrite S[t % 3] once PV(t-3) has read P(t-3) from it, so the
+// scores run up to three tiles ahead of the softmax, which goes from one tile
+// to the next without waiting for the tensor core.  The two MMA streams come
+// from two threads: the PV stream waits for each P, the S stream runs ahead
+// and fills the tensor core whenever the PV stream waits or does its
+// bookkeeping.  Only the softmax is on the critical path.
 //
 // The rescale of O by alpha = 2^(m_old - m_new) is done only when the row max
 // of some row in the warp grew by more than 2^8: otherwise m stays and p may
 // reach 2^8, which changes nothing in exact arithmetic (O and l share the same
-// stale max) and keeps fp16/bf16/fp32 far from overflow.
+// stale max) and keeps fp16/bf16/fp32 far from overflow.  A rescale at tile j
+// waits for PV(j-1) to complete.
+//
+// Barrier phases: S(t), P(j) and "PV(j) done" each use three barriers indexed
+// by tile mod 3, so that no waiter can fall two phases behind on the barrier
+// it waits on (every pair of producer and consumer is at most two tiles apart).
 //
 // Every mbarrier wait is bounded (%globaltimer); on expiry the CTA records
 // the timeout in the status word, stops issuing work, waits (bounded) for its
@@ -52,39 +54,44 @@
 
 namespace fa {
 
-constexpr int kFwdThreads = 384;
-constexpr int kWarpTma = 8, kWarpMma = 9;
-constexpr uint32_t kRegsSoftmax = 200;
-constexpr uint32_t kRegsOther = 104;
+constexpr int kFwdThreads = 256;
+constexpr int kWarpTma = 4, kWarpPv = 5, kWarpS = 6;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct FwdCfg {
     static_assert(D == 64 || D == 128, "head dim");
     static constexpr int kBlocks = D / 64;               // 128-byte swizzle blocks per row
-    static constexpr int kQBlockBytes = kFwdBr * 128;    // one 64-column block of a Q tile
+    static constexpr int kQBlockBytes = kFwdBr * 128;    // one 64-column block of the Q tile
     static constexpr int kKVBlockBytes = kFwdBc * 128;   // one 64-column block of a K/V tile
-    static constexpr int kQBytes = kFwdBr * D * 2;       // one Q tile
+    static constexpr int kQBytes = kFwdBr * D * 2;       // the Q tile
     static constexpr int kTileBytes = kFwdBc * D * 2;    // one K or V tile
-    static constexpr int kStages = (D == 128) ? 4 : 8;   // ring slots (K and V alternate)
-    static constexpr int kOffQ = 0;                      // Q_A, then Q_B
-    static constexpr int kOffRing = kFwdTilesPerCta * kQBytes;
-    static constexpr int kOffBar = kOffRing + kStages * kTileBytes;
-    // barriers: q_full, full[S], empty[S], s_full[2], p_full[2], o_final[2], mma_fin
-    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
+    static constexpr int kStages = (D == 128) ? 3 : 6;   // slots per ring (one K ring, one V ring)
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kQBytes;
+    static constexpr int kOffV = kOffK + kStages * kTileBytes;
+    static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+    // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[3], p_full[3],
+    // pv_done[3], o_final, mma_fin[2]
+    static constexpr int kNumBars = 1 + 4 * kStages + 9 + 1 + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
     static constexpr uint32_t kTmemCols = 512;
-    __device__ static constexpr uint32_t tmem_s(int x) { return 128u * x; }
-    __device__ static constexpr uint32_t tmem_o(int x) { return 256u + 128u * x; }
+    __device__ static constexpr uint32_t tmem_s(int b) { return 128u * b; }
+    static constexpr uint32_t kTmemO = 384;
 };
 
 // K/V tile j needs element masks when it crosses the ragged end of K or, under
-// causal masking, holds a key beyond the first row's last visible key.
-__device__ __forceinline__ bool fwd_tile_needs_mask(int j, int q0, int Nq, int Nk, int causal) {
-    const int last_key = (j + 1) * kFwdBc - 1;
-    return (last_key >= Nk) || (causal && last_key > q0 + (Nk - Nq));
+// causal masking, holds a key beyond the first row's last visible key:
+//   (j+1)*Bc - 1 >= Nk  or  (causal and (j+1)*Bc - 1 > q0 + Nk - Nq).
+// Both conditions are monotone in j; this returns the first tile that meets
+// either, so tile j needs masks exactly when j >= fwd_first_masked_tile(...).
+__device__ __forceinline__ int fwd_first_masked_tile(int q0, int Nq, int Nk, int causal) {
+    const int j_tail = Nk / kFwdBc;
+    if (!causal) return j_tail;
+    const int d1 = q0 + (Nk - Nq) + 1;
+    return min(j_tail, d1 <= 0 ? 0 : d1 / kFwdBc);
 }
 
 // K/V tiles that Q rows [q0, q0+128) must visit (0 when the tile holds no row).
@@ -174,7 +181,7 @@ __device__ __noinline__ RowStep softmax_tile_masked(uint32_t s_addr, int c0, int
     return softmax_tile<true, BF16>(s_addr, c0, lim, sl2, m, l);
 }
 
-// O_X (32 rows of this warp, kCols columns) *= alpha, 16 columns at a time.
+// O (32 rows of this warp, kCols columns) *= alpha, 16 columns at a time.
 // Rarely taken (only when a row max grows by more than 2^8).
 template <int kCols>
 __device__ __noinline__ void rescale_o(uint32_t o_addr, float alpha) {
@@ -211,36 +218,43 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // Consecutive CTAs take consecutive row blocks of one head, heaviest causal
     // block first, so the CTAs resident at any time share a few heads' K/V in L2.
     const int bh = blockIdx.y;
-    const int q0 = (args.num_m - 1 - (int)blockIdx.x) * (kFwdTilesPerCta * kFwdBr);
+    const int q0 = (args.num_m - 1 - (int)blockIdx.x) * kFwdBr;
     const int Nq = args.Nq, Nk = args.Nk, causal = args.causal;
-    const int nA = fwd_tile_count(q0, Nq, Nk, causal);
-    const int nB = fwd_tile_count(q0 + kFwdBr, Nq, Nk, causal);
-    const int n_max = max(nA, nB);
+    const int n = fwd_tile_count(q0, Nq, Nk, causal);
+    const int jm = fwd_first_masked_tile(q0, Nq, Nk, causal);
 
     auto bar = [&](int idx) -> uint32_t { return sb + C::kOffBar + 8u * (uint32_t)idx; };
+    constexpr int S_ = C::kStages;
     constexpr int B_QFULL = 0;
-    auto B_FULL = [](int s) { return 1 + s; };
-    auto B_EMPTY = [](int s) { return 1 + C::kStages + s; };
-    auto B_SFULL = [](int x) { return 1 + 2 * C::kStages + x; };   // S_X(j) in TMEM
-    auto B_PFULL = [](int x) { return 3 + 2 * C::kStages + x; };   // P_X(j) in TMEM (one arrival per warp)
-    auto B_OFINAL = [](int x) { return 5 + 2 * C::kStages + x; };  // last PV_X complete
-    constexpr int B_MMAFIN = 7 + 2 * C::kStages;
+    auto B_KFULL = [](int s) { return 1 + s; };
+    auto B_KEMPTY = [](int s) { return 1 + S_ + s; };
+    auto B_VFULL = [](int s) { return 1 + 2 * S_ + s; };
+    auto B_VEMPTY = [](int s) { return 1 + 3 * S_ + s; };
+    auto B_SFULL = [](int b) { return 1 + 4 * S_ + b; };   // S(t) in S[b], b = t % 3
+    auto B_PFULL = [](int b) { return 4 + 4 * S_ + b; };   // P(j) in S[b] (one arrival per softmax warp)
+    auto B_PVDONE = [](int b) { return 7 + 4 * S_ + b; };  // PV(j) complete, b = j % 3
+    constexpr int B_OFINAL = 10 + 4 * S_;                  // last PV complete
+    auto B_MMAFIN = [](int w) { return 11 + 4 * S_ + w; }; // every MMA of issuer w complete
     volatile uint32_t *tmem_holder = reinterpret_cast<volatile uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
     int *status = args.status;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B_QFULL), 1);
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(bar(B_FULL(s)), 1);
-            mbar_init(bar(B_EMPTY(s)), 1);
+        for (int s = 0; s < S_; ++s) {
+            mbar_init(bar(B_KFULL(s)), 1);
+            mbar_init(bar(B_KEMPTY(s)), 1);
+            mbar_init(bar(B_VFULL(s)), 1);
+            mbar_init(bar(B_VEMPTY(s)), 1);
         }
-        for (int x = 0; x < 2; ++x) {
-            mbar_init(bar(B_SFULL(x)), 1);
-            mbar_init(bar(B_PFULL(x)), 4);
-            mbar_init(bar(B_OFINAL(x)), 1);
+        for (int b = 0; b < 3; ++b) {
+            mbar_init(bar(B_SFULL(b)), 1);
+            mbar_init(bar(B_PFULL(b)), 4);
+            mbar_init(bar(B_PVDONE(b)), 1);
         }
-        mbar_init(bar(B_MMAFIN), 1);
+        mbar_init(bar(B_OFINAL), 1);
+        mbar_init(bar(B_MMAFIN(0)), 1);
+        mbar_init(bar(B_MMAFIN(1)), 1);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -248,7 +262,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
     }
-    if (warp == kWarpMma) {
+    if (warp == kWarpPv) {
         tmem_alloc(sb + C::kOffMisc, C::kTmemCols);
         tmem_relinquish();
     }
@@ -256,154 +270,147 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    constexpr uint32_t hi = sdesc_hi_sw128(1024);  // 8 rows x 128 B per core group
 
-    if (warp >= 8) {
-        regs_decrease<kRegsOther>();
-        if (warp == kWarpTma && lane == 0 && n_max > 0) {
-            // ------------------------------------------------------------ TMA producer
-            uint32_t pend_mask = 0, pend_par = 0;
-            mbar_arrive_expect_tx(bar(B_QFULL), kFwdTilesPerCta * C::kQBytes);
-            for (int x = 0; x < kFwdTilesPerCta; ++x)
+    if (warp == kWarpTma) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && n > 0) {
+            uint32_t pend_k = 0, pend_v = 0;  // slots with a load issued, per ring
+            uint32_t par_k = 0, par_v = 0;    // phase parity of the last load into each slot
+            mbar_arrive_expect_tx(bar(B_QFULL), C::kQBytes);
+            for (int b = 0; b < C::kBlocks; ++b)
+                tma_load_3d(sb + C::kOffQ + b * C::kQBlockBytes, &tmQ, b * 64, q0, bh, bar(B_QFULL));
+            // Tile `tile` of K (V) goes to slot tile % S of its ring, in the order the two
+            // MMA streams consume them: K_0, K_1, K_2, then V_j, K_{j+3} for j = 0, 1, ...
+            auto load = [&](bool is_v, int tile) -> bool {
+                const int s = tile % S_;
+                const uint32_t it = (uint32_t)(tile / S_);
+                if (!mbar_wait_bounded(bar(is_v ? B_VEMPTY(s) : B_KEMPTY(s)), (it & 1u) ^ 1u, abort_flag, status))
+                    return false;
+                const uint32_t full = bar(is_v ? B_VFULL(s) : B_KFULL(s));
+                mbar_arrive_expect_tx(full, C::kTileBytes);
+                const uint32_t dst = sb + (is_v ? C::kOffV : C::kOffK) + s * C::kTileBytes;
                 for (int b = 0; b < C::kBlocks; ++b)
-                    tma_load_3d(sb + C::kOffQ + x * C::kQBytes + b * C::kQBlockBytes, &tmQ, b * 64,
-                                q0 + x * kFwdBr, bh, bar(B_QFULL));
-            // Slot t holds K_{t/2} (t even) or V_{t/2} (t odd).
-            for (int t = 0; t < 2 * n_max; ++t) {
-                const int s = t % C::kStages;
-                const uint32_t it = (uint32_t)(t / C::kStages);
-                if (!mbar_wait_bounded(bar(B_EMPTY(s)), (it & 1u) ^ 1u, abort_flag, status)) break;
-                mbar_arrive_expect_tx(bar(B_FULL(s)), C::kTileBytes);
-                const CUtensorMap *map = (t & 1) ? &tmV : &tmK;
-                const uint32_t dst = sb + C::kOffRing + s * C::kTileBytes;
-                for (int b = 0; b < C::kBlocks; ++b)
-                    tma_load_3d(dst + b * C::kKVBlockBytes, map, b * 64, (t >> 1) * kFwdBc, bh, bar(B_FULL(s)));
-                pend_mask |= 1u << s;
-                pend_par = (pend_par & ~(1u << s)) | ((it & 1u) << s);
-            }
+                    tma_load_3d(dst + b * C::kKVBlockBytes, is_v ? &tmV : &tmK, b * 64, tile * kFwdBc, bh, full);
+                (is_v ? pend_v : pend_k) |= 1u << s;
+                uint32_t &par = is_v ? par_v : par_k;
+                par = (par & ~(1u << s)) | ((it & 1u) << s);
+                return true;
+            };
+            bool ok = true;
+            for (int t = 0; ok && t < min(n, 3); ++t) ok = load(false, t);
+            for (int j = 0; ok && j < n; ++j) ok = load(true, j) && (j + 3 >= n || load(false, j + 3));
             // Every load issued must land before the CTA may exit.
             volatile int no_abort = 0;
             mbar_wait_bounded(bar(B_QFULL), 0, &no_abort, status);
-            for (int s = 0; s < C::kStages; ++s)
-                if (pend_mask & (1u << s)) mbar_wait_bounded(bar(B_FULL(s)), (pend_par >> s) & 1u, &no_abort, status);
-        } else if (warp == kWarpMma && lane == 0 && n_max > 0) {
-            // ------------------------------------------------------------ MMA issuer
+            for (int s = 0; s < S_; ++s) {
+                if (pend_k & (1u << s)) mbar_wait_bounded(bar(B_KFULL(s)), (par_k >> s) & 1u, &no_abort, status);
+                if (pend_v & (1u << s)) mbar_wait_bounded(bar(B_VFULL(s)), (par_v >> s) & 1u, &no_abort, status);
+            }
+        }
+    } else if (warp == kWarpS) {
+        // ------------------------------------------------------------ MMA issuer: S stream
+        if (lane == 0 && n > 0) {
             constexpr uint32_t idesc_qk = idesc_f16(128, kFwdBc, BF16, false);
-            constexpr uint32_t idesc_pv = idesc_f16(128, D, BF16, true);
-            // Descriptors are built once; per instruction only the address field of the
-            // low word moves (by a compile-time offset plus the slot offset).
-            constexpr uint32_t hi = sdesc_hi_sw128(1024);                        // 8 rows x 128 B per core group
-            const uint32_t q_lo = sdesc_lo(sb + C::kOffQ, 16);                   // K-major: LBO unused
-            const uint32_t k_lo = sdesc_lo(sb + C::kOffRing, 16);
-            const uint32_t v_lo = sdesc_lo(sb + C::kOffRing, C::kKVBlockBytes);  // MN-major: LBO = 64-col block
-            auto slot_off = [](int t) { return (uint32_t)((t % C::kStages) * (C::kTileBytes >> 4)); };
-            auto wait_slot = [&](int t) {
-                return mbar_wait_bounded(bar(B_FULL(t % C::kStages)), (uint32_t)(t / C::kStages) & 1u, abort_flag,
-                                         status);
-            };
-            // S_X = Q_X K^T for the K tile in slot t: K-major A and B, 16 of the d
-            // columns per instruction; its commit also covers every earlier MMA.
-            auto issue_s = [&](int x, int t) {
-                const uint32_t qx_lo = q_lo + x * (C::kQBytes >> 4);
-                const uint32_t kt_lo = k_lo + slot_off(t);
-                const uint32_t d_s = tmem + C::tmem_s(x);
+            const uint32_t q_lo = sdesc_lo(sb + C::kOffQ, 16);  // K-major: LBO unused
+            const uint32_t k_lo = sdesc_lo(sb + C::kOffK, 16);
+            bool ok = mbar_wait_bounded(bar(B_QFULL), 0, abort_flag, status);
+            for (int t = 0; ok && t < n; ++t) {
+                const int b = t % 3, s = t % S_;
+                // S[b] is free once PV(t-3) has read P(t-3) from it.
+                if (t >= 3) ok = mbar_wait_bounded(bar(B_PVDONE(b)), (uint32_t)(t / 3 - 1) & 1u, abort_flag, status);
+                ok = ok && mbar_wait_bounded(bar(B_KFULL(s)), (uint32_t)(t / S_) & 1u, abort_flag, status);
+                if (!ok) break;
+                tc_fence_after();
+                // S(t) = Q K_t^T: K-major A and B, 16 of the d columns per instruction.
+                const uint32_t kt_lo = k_lo + (uint32_t)(s * (C::kTileBytes >> 4));
+                const uint32_t d_s = tmem + C::tmem_s(b);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off_q = ((k >> 2) * C::kQBlockBytes + (k & 3) * 32) >> 4;
                     const uint32_t off_k = ((k >> 2) * C::kKVBlockBytes + (k & 3) * 32) >> 4;
-                    umma_ss_w(d_s, qx_lo + off_q, hi, kt_lo + off_k, hi, idesc_qk, k > 0 ? 1u : 0u);
+                    umma_ss_w(d_s, q_lo + off_q, hi, kt_lo + off_k, hi, idesc_qk, k > 0 ? 1u : 0u);
                 }
-                umma_commit(bar(B_SFULL(x)));
-            };
-            // O_X += P_X(j) V_j: P from TMEM (the remainder too on masked tiles), V as an
-            // MN-major operand, 16 keys per instruction.
-            auto issue_pv = [&](int x, int j, int t) {
-                const uint32_t vt_lo = v_lo + slot_off(t);
-                const uint32_t d_o = tmem + C::tmem_o(x);
-                const uint32_t p_t = tmem + C::tmem_s(x);
+                umma_commit(bar(B_SFULL(b)));
+                umma_commit(bar(B_KEMPTY(s)));
+            }
+            // Tensor memory may be freed only after every issued MMA completed.
+            umma_commit(bar(B_MMAFIN(1)));
+            volatile int no_abort = 0;
+            mbar_wait_bounded(bar(B_MMAFIN(1)), 0, &no_abort, status);
+        }
+    } else if (warp == kWarpPv) {
+        // ------------------------------------------------------------ MMA issuer: PV stream
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t idesc_pv = idesc_f16(128, D, BF16, true);
+            const uint32_t v_lo = sdesc_lo(sb + C::kOffV, C::kKVBlockBytes);  // MN-major: LBO = 64-col block
+            const uint32_t d_o = tmem + C::kTmemO;
+            bool ok = true;
+            for (int j = 0; ok && j < n; ++j) {
+                const int b = j % 3, s = j % S_;
+                ok = mbar_wait_bounded(bar(B_PFULL(b)), (uint32_t)(j / 3) & 1u, abort_flag, status) &&
+                     mbar_wait_bounded(bar(B_VFULL(s)), (uint32_t)(j / S_) & 1u, abort_flag, status);
+                if (!ok) break;
+                tc_fence_after();
+                // O += P(j) V_j: P from S[b] (the remainder too on masked tiles), V as an
+                // MN-major operand, 16 keys per instruction.
+                const uint32_t vt_lo = v_lo + (uint32_t)(s * (C::kTileBytes >> 4));
+                const uint32_t p_t = tmem + C::tmem_s(b);
 #pragma unroll
                 for (int k = 0; k < kFwdBc / 16; ++k)
                     umma_ts_w(d_o, p_t + 8 * k, vt_lo + ((k * 2048) >> 4), hi, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
-                if (fwd_tile_needs_mask(j, q0 + x * kFwdBr, Nq, Nk, causal)) {
+                if (j >= jm) {
 #pragma unroll
                     for (int k = 0; k < kFwdBc / 16; ++k)
                         umma_ts_w(d_o, p_t + 64 + 8 * k, vt_lo + ((k * 2048) >> 4), hi, idesc_pv, 1u);
                 }
-            };
-            bool ok = mbar_wait_bounded(bar(B_QFULL), 0, abort_flag, status) && wait_slot(0);
-            if (ok) {
-                tc_fence_after();
-                if (nA > 0) issue_s(0, 0);
-                if (nB > 0) issue_s(1, 0);
-                umma_commit(bar(B_EMPTY(0)));
+                umma_commit(bar(B_PVDONE(b)));
+                umma_commit(bar(B_VEMPTY(s)));
             }
-            for (int j = 0; ok && j < n_max; ++j) {
-                const int tv = 2 * j + 1, tk = 2 * j + 2;  // slots of V_j and K_{j+1}
-                bool v_ready = false, k_ready = false;
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    const int nx = x == 0 ? nA : nB;
-                    if (j >= nx) continue;
-                    // P_X(j) first: it is the wait most likely to block.
-                    ok = mbar_wait_bounded(bar(B_PFULL(x)), (uint32_t)j & 1u, abort_flag, status);
-                    if (ok && !v_ready) ok = v_ready = wait_slot(tv);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(x, j, tv);
-                    if (j + 1 < nx) {
-                        if (!k_ready) {
-                            ok = k_ready = wait_slot(tk);
-                            if (!ok) break;
-                            tc_fence_after();
-                        }
-                        issue_s(x, tk);
-                    } else {
-                        umma_commit(bar(B_OFINAL(x)));
-                    }
-                }
-                if (!ok) break;
-                umma_commit(bar(B_EMPTY(tv % C::kStages)));
-                if (j + 1 < n_max) umma_commit(bar(B_EMPTY(tk % C::kStages)));
-            }
-            // Tensor memory may be freed only after every issued MMA completed.
-            umma_commit(bar(B_MMAFIN));
+            if (ok) umma_commit(bar(B_OFINAL));
+            umma_commit(bar(B_MMAFIN(0)));
             volatile int no_abort = 0;
-            mbar_wait_bounded(bar(B_MMAFIN), 0, &no_abort, status);
+            mbar_wait_bounded(bar(B_MMAFIN(0)), 0, &no_abort, status);
         }
-    } else {
+    } else if (warp < 4) {
         // ------------------------------------------------------------ softmax / correction / epilogue
-        regs_increase<kRegsSoftmax>();
-        const int x = warp >> 2;       // Q tile of this warp
-        const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter+32) belong to this warp
-        const int qx = q0 + x * kFwdBr;
-        const int i = qx + quarter * 32 + lane;
-        const int n_tiles = x == 0 ? nA : nB;
+        const int quarter = warp;  // TMEM lanes [32*quarter, 32*quarter+32) belong to this warp
+        const int i = q0 + quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t s_addr = lane_base + C::tmem_s(x);
-        const uint32_t o_addr = lane_base + C::tmem_o(x);
+        const uint32_t o_addr = lane_base + C::kTmemO;
         const int lim = causal ? min(i + (Nk - Nq), Nk - 1) : Nk - 1;  // last key row i may see
         const float sl2 = args.scale_log2;
         float m = -INFINITY;  // running (possibly stale) max of scale*log2(e)*s
         float l = 0.f;        // running sum of 2^(scale*log2(e)*s - m)
         bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_SFULL(x)), (uint32_t)j & 1u, abort_flag, status));
+        for (int j = 0; j < n; ++j) {
+            const int b = j % 3;
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait_bounded(bar(B_SFULL(b)), (uint32_t)(j / 3) & 1u, abort_flag, status));
             if (!ok) break;
             tc_fence_after();
+            const uint32_t s_addr = lane_base + C::tmem_s(b);
             // Two instances of the same step, so the unmasked (common) tile carries no
             // predicated mask or remainder instructions.
-            const RowStep r = fwd_tile_needs_mask(j, qx, Nq, Nk, causal)
-                                  ? softmax_tile_masked<BF16>(s_addr, j * kFwdBc, lim, sl2, m, l)
-                                  : softmax_tile<false, BF16>(s_addr, 0, 0, sl2, m, l);
+            const RowStep r = j >= jm ? softmax_tile_masked<BF16>(s_addr, j * kFwdBc, lim, sl2, m, l)
+                                      : softmax_tile<false, BF16>(s_addr, 0, 0, sl2, m, l);
             m = r.m;
             l = r.l;
-            if (r.rescale && j > 0) rescale_o<D>(o_addr, r.alpha);  // O_X holds PV_X(0..j-1), all complete
+            if (r.rescale && j > 0) {
+                // O must hold PV(0..j-1) in full before it is scaled.
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_PVDONE((j - 1) % 3)), (uint32_t)((j - 1) / 3) & 1u,
+                                                               abort_flag, status));
+                if (!ok) break;
+                tc_fence_after();
+                rescale_o<D>(o_addr, r.alpha);
+            }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_PFULL(x)));
+            if (lane == 0) mbar_arrive(bar(B_PFULL(b)));
         }
-        if (ok && n_tiles > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_OFINAL(x)), 0, abort_flag, status));
+        if (ok && n > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_OFINAL), 0, abort_flag, status));
             tc_fence_after();
         }
         if (ok && __any_sync(0xffffffffu, i < Nq)) {
@@ -414,7 +421,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t ov[32];
-                if (n_tiles > 0) {
+                if (n > 0) {
                     tmem_ld_32x32b_x32(o_addr + 32 * c, ov);
                     tmem_wait_ld();
                 } else {
@@ -440,7 +447,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == kWarpPv) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);

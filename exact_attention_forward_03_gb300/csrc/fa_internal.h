@@ -12,10 +12,10 @@ namespace fa {
 constexpr int kDevErrTimeout = 1;
 
 // Tile shape of the fused forward kernel: 128 query rows per Q tile (one TMEM
-// lane per row), two Q tiles per CTA, 128 keys per K/V tile.
+// lane per row), one Q tile per CTA, 128 keys per K/V tile.
 constexpr int kFwdBr = 128;
 constexpr int kFwdBc = 128;
-constexpr int kFwdTilesPerCta = 2;
+constexpr int kFwdTilesPerCta = 1;
 // Keys per tile of the split-KV kernel; split lengths are multiples of it.
 constexpr int kDecBc = 64;
 constexpr int kMaxSplits = 256;
