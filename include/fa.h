@@ -73,7 +73,7 @@ typedef enum {
 } fa_status;
 
 /*
- * Fused attention forward (one launch): one CTA per 256 query rows and head,
+ * Fused attention forward (one launch): one CTA per 128 query rows and head,
  * K/V tiles streamed by TMA, both GEMMs on tcgen05 tensor cores with fp32
  * accumulators in tensor memory, online softmax with deferred 1/l.  Under
  * causal masking, K/V tiles entirely above the diagonal are skipped and only
