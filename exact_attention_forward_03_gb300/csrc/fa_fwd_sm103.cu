@@ -36,11 +36,13 @@
 // and fills the tensor core whenever the PV stream waits or does its
 // bookkeeping.  Only the softmax is on the critical path.
 //
-// The rescale of O by alpha = 2^(m_old - m_new) is done only when the row max
-// of some row in the warp grew by more than 2^8: otherwise m stays and p may
-// reach 2^8, which changes nothing in exact arithmetic (O and l share the same
-// stale max) and keeps fp16/bf16/fp32 far from overflow.  A rescale at tile j
-// waits for PV(j-1) to complete.
+// The running max m only keeps p in range: O and l share it, so a stale m
+// changes nothing in exact arithmetic.  The exact row max is taken on a row's
+// first tile and on masked tiles, where m moves (and O is rescaled by
+// alpha = 2^(m_old - m_new)) only if the max grew by more than 2^8; on the
+// other tiles the exponentials are taken against the current m at once and the
+// tile's row sum checks them (see softmax_tile).  A rescale at tile j waits for
+// PV(j-1) to complete.
 //
 // Barrier phases: S(t), P(j) and "PV(j) done" each use three barriers indexed
 // by tile mod 3, so that no waiter can fall two phases behind on the barrier
@@ -57,6 +59,7 @@ namespace fa {
 constexpr int kFwdThreads = 256;
 constexpr int kWarpTma = 4, kWarpPv = 5, kWarpS = 6;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kRowSumLimit = 32768.0f;   // 2^15
 
 template <int D>
 struct FwdCfg {
@@ -110,43 +113,24 @@ struct RowStep {
     bool rescale;  // whether the warp moved its max in this step
 };
 
-// One online-softmax step of this thread's row over one K/V tile: S (128 fp32
-// columns of TMEM at s_addr) into registers, optional causal/tail mask,
-// (conditional) max update, p = 2^(s*c - m), the row sum, and P written back
-// as 16-bit pairs over the first 64 columns (the 16-bit remainder over the
-// next 64 on masked tiles).  Keys [16k, 16k+16) land in columns [8k, 8k+8).
-template <bool MASKED, bool BF16>
-__device__ __forceinline__ RowStep softmax_tile(uint32_t s_addr, int c0, int lim, float sl2, float m, float l) {
-    using PK = Pack<BF16>;
-    uint32_t s[128];
-    tmem_ld_32x32b_x32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-    tmem_ld_32x32b_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-    tmem_ld_32x32b_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-    tmem_ld_32x32b_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-    tmem_wait_ld();
-    if (MASKED) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-            if (c0 + c > lim) s[c] = __float_as_uint(-INFINITY);
-    }
+// Largest of the row's 128 scores (fp32 bits; -inf entries count as -inf).
+__device__ __forceinline__ float row_max(const uint32_t (&s)[128]) {
     float mx[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) mx[e] = fmax3(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), -INFINITY);
 #pragma unroll
     for (int c = 16; c < 128; c += 2)
         mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
-    const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-    const float m_cand = fmaxf(m, mt * sl2);
-    RowStep r;
-    r.rescale = __any_sync(0xffffffffu, m_cand > m + kRescaleThreshold);
-    r.alpha = 1.f;
-    if (r.rescale) {
-        const float m_new_d = (m_cand == -INFINITY) ? 0.f : m_cand;  // never subtract -inf from -inf
-        r.alpha = ex2_approx(m - m_new_d);
-        m = m_cand;
-    }
-    r.m = m;
-    const float m_d = (m == -INFINITY) ? 0.f : m;
+    return fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+}
+
+// p = 2^(s*c - m_d) for the row's 128 scores, written as 16-bit pairs over the
+// first 64 TMEM columns at s_addr (keys [16k, 16k+16) in columns [8k, 8k+8);
+// on masked tiles the 16-bit remainder p - p_head over the next 64); returns
+// the fp32 sum of the p.
+template <bool MASKED, bool BF16>
+__device__ __forceinline__ float exp_row(const uint32_t (&s)[128], uint32_t s_addr, float sl2, float m_d) {
+    using PK = Pack<BF16>;
     const uint64_t scale2 = f2_make(sl2, sl2);
     const uint64_t shift2 = f2_make(-m_d, -m_d);
     uint64_t rs2[4] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f), f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
@@ -170,7 +154,60 @@ __device__ __forceinline__ RowStep softmax_tile(uint32_t s_addr, int c0, int lim
         if (MASKED) tmem_st_32x32b_x16(s_addr + 64 + 16 * c, pl);
     }
     const float2 r0 = f2_split(fadd2(rs2[0], rs2[1])), r1 = f2_split(fadd2(rs2[2], rs2[3]));
-    r.l = l * r.alpha + ((r0.x + r0.y) + (r1.x + r1.y));
+    return (r0.x + r0.y) + (r1.x + r1.y);
+}
+
+// One online-softmax step of this thread's row over one K/V tile: S (128 fp32
+// columns of TMEM at s_addr) into registers, optional causal/tail mask, the
+// exponentials against the running max m, the row sum, and P over the first
+// 64 columns of S (see exp_row).
+//
+// Any finite m gives the same O and l in exact arithmetic (O and l are both
+// relative to it), so m only has to keep p within range.  The exact row max is
+// taken on a row's first tile and on masked tiles (where a max that grew by
+// more than 2^8 moves m and rescales O).  On the other tiles the exponentials
+// are taken against the current m straight away, with no max pass, and the
+// tile's row sum checks the result: when every row of the warp summed to at
+// most 2^15, every p is at most 2^15 (inside fp16 and bf16) and the tile
+// stands; otherwise (the scores rose well above m) the warp takes the exact
+// max, moves m, and redoes the tile.
+template <bool MASKED, bool BF16>
+__device__ __forceinline__ RowStep softmax_tile(uint32_t s_addr, int c0, int lim, float sl2, float m, float l) {
+    uint32_t s[128];
+    tmem_ld_32x32b_x32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+    tmem_ld_32x32b_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+    tmem_ld_32x32b_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+    tmem_ld_32x32b_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+    tmem_wait_ld();
+    if (MASKED) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+            if (c0 + c > lim) s[c] = __float_as_uint(-INFINITY);
+    }
+    RowStep r;
+    r.rescale = false;
+    r.alpha = 1.f;
+    const bool exact = MASKED || __any_sync(0xffffffffu, m == -INFINITY);
+    if (exact) {
+        const float m_cand = fmaxf(m, row_max(s) * sl2);
+        r.rescale = __any_sync(0xffffffffu, m_cand > m + kRescaleThreshold);
+        if (r.rescale) {
+            const float m_new_d = (m_cand == -INFINITY) ? 0.f : m_cand;  // never subtract -inf from -inf
+            r.alpha = ex2_approx(m - m_new_d);
+            m = m_cand;
+        }
+    }
+    float sum = exp_row<MASKED, BF16>(s, s_addr, sl2, (m == -INFINITY) ? 0.f : m);
+    if (!exact && __any_sync(0xffffffffu, sum > kRowSumLimit)) {
+        // m is finite on every row of the warp here, and m_cand >= m.
+        const float m_cand = fmaxf(m, row_max(s) * sl2);
+        r.alpha = ex2_approx(m - m_cand);
+        r.rescale = true;
+        m = m_cand;
+        sum = exp_row<false, BF16>(s, s_addr, sl2, m);
+    }
+    r.m = m;
+    r.l = l * r.alpha + sum;
     return r;
 }
 

@@ -151,6 +151,24 @@ def test_large_scores_stay_finite(fa):
         compare(o, o_ref, lse, lse_ref, q.dtype, f"large scores causal={causal}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_scores_jump_on_a_later_unmasked_tile(fa, dtype):
+    """Even rows meet keys on tile 5 whose scores sit ~20 (natural-log units) above
+    everything before: the exponentials taken against the running max overshoot
+    there, and those rows (not their odd neighbours in the same warp) must move
+    their max, rescale O and redo the tile."""
+    B, H, Nq, Nk, d = 1, 2, 256, 1024, 128
+    q, k, v = attn_inputs.make_qkv(B, H, Nq, Nk, d, dtype, 41, "cuda")
+    q[:, :, 0::2, 0] += 15.0
+    k[:, :, 640:768, 0] += 15.0
+    for causal in (False, True):
+        o, lse = fa.fwd(q, k, v, causal=causal)
+        torch.cuda.synchronize()
+        assert fa.get_device_status() == fa.FA_OK
+        o_ref, lse_ref = oracle.attention(q, k, v, causal, 1 / math.sqrt(d))
+        compare(o, o_ref, lse, lse_ref, q.dtype, f"score jump {dtype} causal={causal}")
+
+
 def test_lse_optional(fa):
     q, k, v = attn_inputs.make_qkv(1, 1, 130, 130, 64, "f16", 35, "cuda")
     o1, _ = fa.fwd(q, k, v, causal=True, want_lse=False)
