@@ -75,6 +75,27 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// The same wait for threads off the critical path: between polls the thread
+// sleeps about `ns` nanoseconds, leaving the issue slots of its SM sub-partition
+// to the warps that share it.
+__device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity, volatile int *abort, int *status,
+                                                  uint32_t ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        __nanosleep(ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 15u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                atomicOr(status, kDevErrTimeout);
+                return false;
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

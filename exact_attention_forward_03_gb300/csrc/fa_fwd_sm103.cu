@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             auto load = [&](bool is_v, int tile) -> bool {
                 const int s = tile % S_;
                 const uint32_t it = (uint32_t)(tile / S_);
-                if (!mbar_wait_bounded(bar(is_v ? B_VEMPTY(s) : B_KEMPTY(s)), (it & 1u) ^ 1u, abort_flag, status))
+                if (!mbar_wait_backoff(bar(is_v ? B_VEMPTY(s) : B_KEMPTY(s)), (it & 1u) ^ 1u, abort_flag, status, 64))
                     return false;
                 const uint32_t full = bar(is_v ? B_VFULL(s) : B_KFULL(s));
                 mbar_arrive_expect_tx(full, C::kTileBytes);
@@ -355,8 +355,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int t = 0; ok && t < n; ++t) {
                 const int b = t % 3, s = t % S_;
                 // S[b] is free once PV(t-3) has read P(t-3) from it.
-                if (t >= 3) ok = mbar_wait_bounded(bar(B_PVDONE(b)), (uint32_t)(t / 3 - 1) & 1u, abort_flag, status);
-                ok = ok && mbar_wait_bounded(bar(B_KFULL(s)), (uint32_t)(t / S_) & 1u, abort_flag, status);
+                if (t >= 3) ok = mbar_wait_backoff(bar(B_PVDONE(b)), (uint32_t)(t / 3 - 1) & 1u, abort_flag, status, 64);
+                ok = ok && mbar_wait_backoff(bar(B_KFULL(s)), (uint32_t)(t / S_) & 1u, abort_flag, status, 64);
                 if (!ok) break;
                 tc_fence_after();
                 // S(t) = Q K_t^T: K-major A and B, 16 of the d columns per instruction.
@@ -385,8 +385,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             bool ok = true;
             for (int j = 0; ok && j < n; ++j) {
                 const int b = j % 3, s = j % S_;
-                ok = mbar_wait_bounded(bar(B_PFULL(b)), (uint32_t)(j / 3) & 1u, abort_flag, status) &&
-                     mbar_wait_bounded(bar(B_VFULL(s)), (uint32_t)(j / S_) & 1u, abort_flag, status);
+                ok = mbar_wait_backoff(bar(B_PFULL(b)), (uint32_t)(j / 3) & 1u, abort_flag, status, 32) &&
+                     mbar_wait_backoff(bar(B_VFULL(s)), (uint32_t)(j / S_) & 1u, abort_flag, status, 32);
                 if (!ok) break;
                 tc_fence_after();
                 // O += P(j) V_j: P from S[b] (the remainder too on masked tiles), V as an
