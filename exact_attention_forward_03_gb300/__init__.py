@@ -39,7 +39,8 @@ FA_ERR_SCRATCH_LIMIT = -7
 
 EXPORTS = ("fa_fwd", "fa_fwd_splitkv", "fa_splitkv_combine", "fa_splitkv_workspace_bytes",
            "fa_splitkv_num_splits", "fa_splitkv_split_len", "fa_get_device_status", "fa_status_string",
-           "fa_version", "fa_fwd_splitkv_noalloc", "fa_splitkv_noalloc_capacity_bytes")
+           "fa_version", "fa_fwd_splitkv_noalloc", "fa_splitkv_noalloc_capacity_bytes", "fa_fwd_gqa",
+           "fa_fwd_splitkv_gqa")
 
 _lock = threading.Lock()
 _lib = None
@@ -82,6 +83,10 @@ def load_library(path: str | None = None):
         lib.fa_version.restype = i
         lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
         lib.fa_fwd_splitkv_noalloc.restype = i
+        lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd_gqa.restype = i
+        lib.fa_fwd_splitkv_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, vp, sz, vp]
+        lib.fa_fwd_splitkv_gqa.restype = i
         lib.fa_splitkv_noalloc_capacity_bytes.argtypes = []
         lib.fa_splitkv_noalloc_capacity_bytes.restype = sz
         if path is None:
@@ -113,7 +118,8 @@ def _stream_handle(stream) -> int:
     return int(s.cuda_stream)
 
 
-def _check_qkv(q, k, v):
+def _check_qkv(q, k, v, allow_gqa=True):
+    """(B, H, H_kv, Nq, Nk, d) of q [B, H, Nq, d] and k, v [B, H_kv, Nk, d] (H_kv divides H)."""
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
@@ -122,9 +128,11 @@ def _check_qkv(q, k, v):
     if not (q.dtype == k.dtype == v.dtype):
         raise TypeError("q, k and v must share one dtype")
     B, H, Nq, d = q.shape
-    if k.shape[:2] != (B, H) or v.shape != k.shape or k.shape[3] != d:
+    H_kv = k.shape[1]
+    ok_heads = H_kv == H or (allow_gqa and H_kv > 0 and H % H_kv == 0)
+    if k.shape[0] != B or not ok_heads or v.shape != k.shape or k.shape[3] != d:
         raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
-    return B, H, Nq, k.shape[2], d
+    return B, H, H_kv, Nq, k.shape[2], d
 
 
 def _outputs(q, out, lse, B, H, Nq, want_lse=True):
@@ -141,16 +149,21 @@ def _outputs(q, out, lse, B, H, Nq, want_lse=True):
 
 def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, want_lse: bool = True,
         stream=None):
-    """Fused attention forward through ``fa_fwd``.  Returns (o, lse)."""
-    B, H, Nq, Nk, d = _check_qkv(q, k, v)
+    """Fused attention forward through ``fa_fwd`` (``fa_fwd_gqa`` when k and v have
+    fewer heads than q: grouped-query attention).  Returns (o, lse)."""
+    B, H, H_kv, Nq, Nk, d = _check_qkv(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     out, lse = _outputs(q, out, lse, B, H, Nq, want_lse)
     lib = load_library()
-    rc = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                    lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d, int(bool(causal)), scale,
-                    _dtype_code(q), _stream_handle(stream))
+    lse_p = lse.data_ptr() if lse is not None else None
+    if H_kv == H:
+        rc = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_p, B, H, Nq, Nk, d,
+                        int(bool(causal)), scale, _dtype_code(q), _stream_handle(stream))
+    else:
+        rc = lib.fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_p, B, H, H_kv, Nq, Nk, d,
+                            int(bool(causal)), scale, _dtype_code(q), _stream_handle(stream))
     if rc != FA_OK:
-        raise FaError(rc, "fa_fwd")
+        raise FaError(rc, "fa_fwd" if H_kv == H else "fa_fwd_gqa")
     return out, lse
 
 
@@ -177,8 +190,9 @@ def splitkv_workspace(q, k, num_splits=0):
 
 def fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None, num_splits: int = 0, workspace=None,
                 out=None, lse=None, want_lse: bool = True, stream=None):
-    """Split-KV forward (partials + combine) through ``fa_fwd_splitkv``.  Returns (o, lse)."""
-    B, H, Nq, Nk, d = _check_qkv(q, k, v)
+    """Split-KV forward (partials + combine) through ``fa_fwd_splitkv`` (``fa_fwd_splitkv_gqa``
+    when k and v have fewer heads than q).  Returns (o, lse)."""
+    B, H, H_kv, Nq, Nk, d = _check_qkv(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     out, lse = _outputs(q, out, lse, B, H, Nq, want_lse)
     if num_splits <= 0:
@@ -186,12 +200,18 @@ def fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None, num_s
     if workspace is None:
         workspace = splitkv_workspace(q, k, num_splits)
     lib = load_library()
-    rc = lib.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                            lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d, int(bool(causal)), scale,
-                            _dtype_code(q), int(num_splits), workspace.data_ptr(),
-                            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    lse_p = lse.data_ptr() if lse is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if H_kv == H:
+        rc = lib.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_p, B, H, Nq, Nk, d,
+                                int(bool(causal)), scale, _dtype_code(q), int(num_splits), workspace.data_ptr(),
+                                ws_bytes, _stream_handle(stream))
+    else:
+        rc = lib.fa_fwd_splitkv_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse_p, B, H, H_kv, Nq,
+                                    Nk, d, int(bool(causal)), scale, _dtype_code(q), int(num_splits),
+                                    workspace.data_ptr(), ws_bytes, _stream_handle(stream))
     if rc != FA_OK:
-        raise FaError(rc, "fa_fwd_splitkv")
+        raise FaError(rc, "fa_fwd_splitkv" if H_kv == H else "fa_fwd_splitkv_gqa")
     return out, lse
 
 
@@ -199,7 +219,7 @@ def fwd_splitkv_noalloc(q, k, v, causal: bool = False, scale: float | None = Non
                         lse=None, want_lse: bool = True, stream=None):
     """Split-KV forward through ``fa_fwd_splitkv_noalloc``: the partials use the
     library's built-in scratch, so no workspace is passed.  Returns (o, lse)."""
-    B, H, Nq, Nk, d = _check_qkv(q, k, v)
+    B, H, _, Nq, Nk, d = _check_qkv(q, k, v, allow_gqa=False)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     out, lse = _outputs(q, out, lse, B, H, Nq, want_lse)
     lib = load_library()

@@ -132,10 +132,11 @@ const char *fa_status_string(int status) {
     }
 }
 
-int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq, int Nk, int d,
-           int causal, float scale, fa_dtype dtype, fa_stream_t stream) {
+int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int H_kv, int Nq,
+               int Nk, int d, int causal, float scale, fa_dtype dtype, fa_stream_t stream) {
     int rc = check_common(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, dtype);
     if (rc != FA_OK) return rc;
+    if (H_kv <= 0 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     const int num_m = (Nq + kFwdTilesPerCta * kFwdBr - 1) / (kFwdTilesPerCta * kFwdBr);
     if (B * H > 65535) return FA_ERR_INVALID_ARG;  // grid.y limit
     DeviceState *st = nullptr;
@@ -143,8 +144,8 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
     const bool bf16 = dtype == FA_BF16;
     const int BH = B * H;
     CUtensorMap tq, tk, tv;
-    if (make_map(&tq, q, bf16, d, Nq, BH, kFwdBr) != FA_OK || make_map(&tk, k, bf16, d, Nk, BH, kFwdBc) != FA_OK ||
-        make_map(&tv, v, bf16, d, Nk, BH, kFwdBc) != FA_OK)
+    if (make_map(&tq, q, bf16, d, Nq, BH, kFwdBr) != FA_OK || make_map(&tk, k, bf16, d, Nk, B * H_kv, kFwdBc) != FA_OK ||
+        make_map(&tv, v, bf16, d, Nk, B * H_kv, kFwdBc) != FA_OK)
         return FA_ERR_CUDA;
     FwdArgs a;
     a.o = o;
@@ -153,10 +154,17 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
     a.Nq = Nq;
     a.Nk = Nk;
     a.num_m = num_m;
+    a.H = H;
+    a.group = H / H_kv;
     a.causal = causal;
     a.scale_log2 = scale * 1.4426950408889634f;
     cudaError_t e = launch_fwd(d, bf16, tq, tk, tv, a, BH, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq, int Nk, int d,
+           int causal, float scale, fa_dtype dtype, fa_stream_t stream) {
+    return fa_fwd_gqa(q, k, v, o, lse, B, H, H, Nq, Nk, d, causal, scale, dtype, stream);
 }
 
 int fa_splitkv_num_splits(int B, int H, int Nq, int Nk, int d) {
@@ -203,11 +211,12 @@ int fa_splitkv_combine(const float *o_part, const float *lse_part, void *o, floa
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq, int Nk,
-                   int d, int causal, float scale, fa_dtype dtype, int num_splits, void *workspace,
-                   size_t workspace_bytes, fa_stream_t stream) {
+int fa_fwd_splitkv_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int H_kv,
+                       int Nq, int Nk, int d, int causal, float scale, fa_dtype dtype, int num_splits, void *workspace,
+                       size_t workspace_bytes, fa_stream_t stream) {
     int rc = check_common(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, dtype);
     if (rc != FA_OK) return rc;
+    if (H_kv <= 0 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     if (num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
     DeviceState *st = nullptr;
     if ((rc = dev_state(&st)) != FA_OK) return rc;
@@ -217,9 +226,8 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *
     const size_t need = fa_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits);
     if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need) return FA_ERR_WORKSPACE;
     const bool bf16 = dtype == FA_BF16;
-    const int BH = B * H;
     CUtensorMap tk, tv;
-    if (make_map(&tk, k, bf16, d, Nk, BH, kDecBc) != FA_OK || make_map(&tv, v, bf16, d, Nk, BH, kDecBc) != FA_OK)
+    if (make_map(&tk, k, bf16, d, Nk, B * H_kv, kDecBc) != FA_OK || make_map(&tv, v, bf16, d, Nk, B * H_kv, kDecBc) != FA_OK)
         return FA_ERR_CUDA;
     float *o_part = static_cast<float *>(workspace);
     float *lse_part =
@@ -231,7 +239,9 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *
     a.status = st->status;
     a.Nq = Nq;
     a.Nk = Nk;
-    a.BH = BH;
+    a.BH = B * H;
+    a.H = H;
+    a.group = H / H_kv;
     a.num_splits = num_splits;
     a.split_len = fa_splitkv_split_len(Nk, num_splits);
     a.causal = causal;
@@ -240,6 +250,13 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *
     cudaError_t e = launch_splitkv(d, bf16, tk, tv, a, s);
     if (e != cudaSuccess) return FA_ERR_CUDA;
     return fa_splitkv_combine(o_part, lse_part, o, lse, num_splits, B, H, Nq, d, dtype, stream);
+}
+
+int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq, int Nk,
+                   int d, int causal, float scale, fa_dtype dtype, int num_splits, void *workspace,
+                   size_t workspace_bytes, fa_stream_t stream) {
+    return fa_fwd_splitkv_gqa(q, k, v, o, lse, B, H, H, Nq, Nk, d, causal, scale, dtype, num_splits, workspace,
+                              workspace_bytes, stream);
 }
 
 int fa_get_device_status(fa_stream_t stream) {
@@ -302,6 +319,8 @@ int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o,
     a.Nq = Nq;
     a.Nk = Nk;
     a.BH = BH;
+    a.H = H;
+    a.group = 1;
     a.num_splits = num_splits;
     a.split_len = fa_splitkv_split_len(Nk, num_splits);
     a.causal = causal;

@@ -96,6 +96,13 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity,
     }
 }
 
+// K/V head read by query head bh = b*H + h when `group` consecutive query heads
+// share one K/V head (grouped-query attention; group = 1 is plain multi-head):
+// K/V head b*(H/group) + h/group of the [B, H/group, N, d] K and V tensors.
+__device__ __forceinline__ int kv_head(int bh, int H, int group) {
+    return (bh / H) * (H / group) + (bh % H) / group;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int bh = blockIdx.y;
     const int q0 = (args.num_m - 1 - (int)blockIdx.x) * kFwdBr;
     const int Nq = args.Nq, Nk = args.Nk, causal = args.causal;
+    const int kvh = kv_head(bh, args.H, args.group);  // the K/V head this query head reads
     const int n = fwd_tile_count(q0, Nq, Nk, causal);
     const int jm = fwd_first_masked_tile(q0, Nq, Nk, causal);
 
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 mbar_arrive_expect_tx(full, C::kTileBytes);
                 const uint32_t dst = sb + (is_v ? C::kOffV : C::kOffK) + s * C::kTileBytes;
                 for (int b = 0; b < C::kBlocks; ++b)
-                    tma_load_3d(dst + b * C::kKVBlockBytes, is_v ? &tmV : &tmK, b * 64, tile * kFwdBc, bh, full);
+                    tma_load_3d(dst + b * C::kKVBlockBytes, is_v ? &tmV : &tmK, b * 64, tile * kFwdBc, kvh, full);
                 (is_v ? pend_v : pend_k) |= 1u << s;
                 uint32_t &par = is_v ? par_v : par_k;
                 par = (par & ~(1u << s)) | ((it & 1u) << s);

@@ -26,6 +26,8 @@ struct FwdArgs {
     int *status;    // device status word
     int Nq, Nk;
     int num_m;      // ceil(Nq / (kFwdTilesPerCta * kFwdBr)): row blocks per head
+    int H;          // query heads per batch entry
+    int group;      // query heads per K/V head (H / H_kv)
     int causal;
     float scale_log2;  // scale * log2(e)
 };
@@ -36,6 +38,7 @@ struct SplitArgs {
     float *lse_part;   // [S, BH, Nq] fp32
     int *status;
     int Nq, Nk, BH;
+    int H, group;      // query heads per batch entry; query heads per K/V head
     int num_splits, split_len;
     int causal;
     float scale_log2;

@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kSplitThreads)
     const long long rest = idx / a.num_splits;
     const int i = (int)(rest % a.Nq);
     const int bh = (int)(rest / a.Nq);
+    const int kvh = kv_head(bh, a.H, a.group);  // the K/V head this query head reads
     const size_t out_row = (size_t)split * a.BH * a.Nq + (size_t)bh * a.Nq + i;
 
     const int k0 = split * a.split_len;
@@ -89,8 +90,8 @@ __global__ void __launch_bounds__(kSplitThreads)
         const int y = k0 + t * kDecBc;
         mbar_arrive_expect_tx(bar(s), 2 * C::kTileBytes);
         for (int b = 0; b < C::kBlocks; ++b) {
-            tma_load_3d(dst + b * C::kBlockBytes, &tmK, b * 64, y, bh, bar(s));
-            tma_load_3d(dst + C::kTileBytes + b * C::kBlockBytes, &tmV, b * 64, y, bh, bar(s));
+            tma_load_3d(dst + b * C::kBlockBytes, &tmK, b * 64, y, kvh, bar(s));
+            tma_load_3d(dst + C::kTileBytes + b * C::kBlockBytes, &tmV, b * 64, y, kvh, bar(s));
         }
     };
 

@@ -130,6 +130,29 @@ FA_API int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, 
                    fa_stream_t stream);
 
 /*
+ * Grouped-query attention (GQA; multi-query attention when H_kv = 1): H query
+ * heads share H_kv K/V heads, `H / H_kv` consecutive query heads per K/V head,
+ * so query head h of batch entry b reads K/V head h / (H / H_kv) of that entry:
+ *
+ *     O[b,h,i,:] = sum_j softmax_j( scale * q[b,h,i] . k[b,h/g,j] + mask ) v[b,h/g,j],  g = H / H_kv
+ *
+ * Otherwise these are fa_fwd and fa_fwd_splitkv (which are the case H_kv = H):
+ * q, o are [B, H, Nq, d]; k, v are [B, H_kv, Nk, d]; lse is [B, H, Nq]; the
+ * split-KV workspace is sized by fa_splitkv_workspace_bytes(B, H, ...) as for
+ * multi-head attention.  ("Flash Attention (4)" §5: the K/V index mapped per
+ * group of query heads; "Lecture 25" §0.3, its table's GQA entry.)
+ * Errors: as fa_fwd / fa_fwd_splitkv, plus FA_ERR_INVALID_ARG when H_kv <= 0
+ * or H is not a multiple of H_kv.
+ */
+FA_API int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
+           int B, int H, int H_kv, int Nq, int Nk, int d, int causal, float scale,
+           fa_dtype dtype, fa_stream_t stream);
+FA_API int fa_fwd_splitkv_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
+                   int B, int H, int H_kv, int Nq, int Nk, int d, int causal, float scale,
+                   fa_dtype dtype, int num_splits, void *workspace, size_t workspace_bytes,
+                   fa_stream_t stream);
+
+/*
  * LSE-weighted merge of split partials, per row r of B*H*Nq rows:
  *   M = max_s LSE_s;  w_s = exp(LSE_s - M);
  *   O = sum_s w_s O_s / sum_s w_s;  LSE = M + ln sum_s w_s.

@@ -189,6 +189,31 @@ def attention_rows(q_rows, row_index, kv_slot, k, v, Nq: int, causal: bool, scal
     return o, lse
 
 
+def kv_head_of(bh: int, H: int, H_kv: int) -> int:
+    """K/V head read by query head bh = b*H + h under grouped-query attention:
+    H // H_kv consecutive query heads share one K/V head, so it is b*H_kv + h // (H // H_kv)
+    ("Flash Attention (4)" §5: the K/V index mapped per group of query heads)."""
+    return (bh // H) * H_kv + (bh % H) // (H // H_kv)
+
+
+def attention_gqa(q, k, v, causal: bool, scale: float, lib=None):
+    """Exact grouped-query attention.  q: [B, H, Nq, d]; k, v: [B, H_kv, Nk, d] with H_kv
+    dividing H -> (O [B, H, Nq, d], LSE [B, H, Nq]).  Every query row is the plain
+    definition (attention_rows) against the K/V head of its group; H_kv = H is
+    multi-head attention and H_kv = 1 multi-query attention."""
+    q64, k64, v64 = to_f64(q), to_f64(k), to_f64(v)
+    B, H, Nq, d = q64.shape
+    H_kv, Nk = k64.shape[1], k64.shape[2]
+    if H_kv <= 0 or H % H_kv != 0 or k64.shape != v64.shape or k64.shape[0] != B or k64.shape[3] != d:
+        raise ValueError("attention_gqa: k, v must be [B, H_kv, Nk, d] with H_kv dividing H")
+    bh = np.repeat(np.arange(B * H), Nq)
+    rows = np.tile(np.arange(Nq), B * H)
+    slots = np.array([kv_head_of(int(x), H, H_kv) for x in range(B * H)], dtype=np.int64)[bh]
+    o, lse = attention_rows(q64.reshape(B * H * Nq, d), rows, slots, k64.reshape(B * H_kv, Nk, d),
+                            v64.reshape(B * H_kv, Nk, d), Nq, causal, scale, lib=lib)
+    return o.reshape(B, H, Nq, d), lse.reshape(B, H, Nq)
+
+
 def sampled_rows(q, k, v, pairs, causal: bool, scale: float, heads_per_batch: int = 16):
     """Oracle values for the (bh, row) pairs of ``[B, H, N, d]`` tensors (any device).
 
@@ -198,6 +223,7 @@ def sampled_rows(q, k, v, pairs, causal: bool, scale: float, heads_per_batch: in
     """
     d = q.shape[-1]
     Nq = q.shape[-2]
+    H, H_kv = q.shape[1], k.shape[1]  # H_kv < H: grouped-query attention (kv_head_of)
     qf = q.reshape(-1, Nq, d)
     kf = k.reshape(-1, k.shape[-2], d)
     vf = v.reshape(-1, v.shape[-2], d)
@@ -209,8 +235,8 @@ def sampled_rows(q, k, v, pairs, causal: bool, scale: float, heads_per_batch: in
     bhs = sorted(by_bh)
     for s in range(0, len(bhs), heads_per_batch):
         group = bhs[s:s + heads_per_batch]
-        kk = np.stack([to_f64(kf[bh]) for bh in group])
-        vv = np.stack([to_f64(vf[bh]) for bh in group])
+        kk = np.stack([to_f64(kf[kv_head_of(bh, H, H_kv)]) for bh in group])
+        vv = np.stack([to_f64(vf[kv_head_of(bh, H, H_kv)]) for bh in group])
         idx, rows, slots, qr = [], [], [], []
         for slot, bh in enumerate(group):
             for n in by_bh[bh]:

@@ -63,6 +63,19 @@ def test_validation_without_gpu(lib):
     assert c(p, p, p, None, 4, 1, 1, 1, 32, 0, None) == -2
 
 
+def test_gqa_head_counts_are_checked_without_gpu(lib):
+    """H must be a positive multiple of H_kv; checked before any CUDA call."""
+    p = ctypes.c_void_p(1 << 20)
+    g = lib.fa_fwd_gqa
+    assert g(p, p, p, p, None, 1, 8, 3, 8, 8, 64, 0, 0.125, 0, None) == -1   # 8 % 3 != 0
+    assert g(p, p, p, p, None, 1, 8, 0, 8, 8, 64, 0, 0.125, 0, None) == -1   # H_kv = 0
+    assert g(p, p, p, p, None, 1, 8, -2, 8, 8, 64, 0, 0.125, 0, None) == -1  # H_kv < 0
+    assert g(p, p, p, p, None, 1, 8, 2, 8, 8, 96, 0, 0.125, 0, None) == -2   # the common checks still apply
+    s = lib.fa_fwd_splitkv_gqa
+    assert s(p, p, p, p, None, 1, 6, 4, 1, 64, 64, 0, 0.125, 0, 4, p, 1 << 20, None) == -1
+    assert s(p, p, p, p, None, 1, 6, 0, 1, 64, 64, 0, 0.125, 0, 4, p, 1 << 20, None) == -1
+
+
 def test_split_planning(lib):
     assert lib.fa_splitkv_split_len(16384, 16) == 1024
     assert lib.fa_splitkv_split_len(1000, 8) == 128
