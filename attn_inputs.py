@@ -36,6 +36,11 @@ class Workload:
     dtype: str
     causal: bool
     seed: int
+    H_kv: int = 0  # K/V heads (grouped-query attention); 0 means H
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H_kv or self.H
 
     @property
     def scale(self) -> float:
@@ -54,7 +59,7 @@ class Workload:
         """Bytes every implementation must move: Q, K, V read, O written (16-bit), LSE written (fp32)."""
         e = 2
         q = self.B * self.H * self.Nq * self.d * e
-        kv = 2 * self.B * self.H * self.Nk * self.d * e
+        kv = 2 * self.B * self.kv_heads * self.Nk * self.d * e
         o = q
         lse = self.B * self.H * self.Nq * 4
         return q + kv + o + lse
@@ -70,6 +75,9 @@ WORKLOADS = {
     "b2h32_n8192_d128_bf16": Workload("b2h32_n8192_d128_bf16", 2, 32, 8192, 8192, 128, "bf16", False, 3000),
     "b1h32_n32768_d128_bf16_causal": Workload("b1h32_n32768_d128_bf16_causal", 1, 32, 32768, 32768, 128, "bf16", True, 4000),
     "decode_b32h32_nk16384_d128_bf16": Workload("decode_b32h32_nk16384_d128_bf16", 32, 32, 1, 16384, 128, "bf16", False, 5000),
+    # Grouped-query decode: 32 query heads over 8 K/V heads (4 per group).
+    "decode_b32h32kv8_nk16384_d128_bf16": Workload("decode_b32h32kv8_nk16384_d128_bf16", 32, 32, 1, 16384, 128, "bf16",
+                                                   False, 6000, H_kv=8),
 }
 
 
@@ -98,7 +106,13 @@ def make_qkv(B: int, H: int, Nq: int, Nk: int, d: int, dtype="f16", seed: int = 
 
 
 def make_workload(w: Workload, device="cpu"):
-    return make_qkv(w.B, w.H, w.Nq, w.Nk, w.d, w.dtype, w.seed, device)
+    if w.kv_heads == w.H:
+        return make_qkv(w.B, w.H, w.Nq, w.Nk, w.d, w.dtype, w.seed, device)
+    tdt = DTYPES[w.dtype]
+    q = _randn((w.B, w.H, w.Nq, w.d), tdt, w.seed + 1, device)
+    k = _randn((w.B, w.kv_heads, w.Nk, w.d), tdt, w.seed + 2, device)
+    v = _randn((w.B, w.kv_heads, w.Nk, w.d), tdt, w.seed + 3, device)
+    return q, k, v
 
 
 def sample_rows(Nq: int, BH: int, count: int, seed: int, tile: int = 128):

@@ -7,7 +7,8 @@ bf16 inputs drawn N(0,1) from fixed seeds, scale 1/sqrt(d).  The headline
 causal, timed with CUDA events around every fa_fwd launch on the launching
 stream, with the L2 cache flushed (a 256 MiB write) before each timed launch.
 The split-KV decode path (B=32, H=32, Nq=1, Nk=16384, d=128, bf16, 16 splits)
-is timed the same way and reported under "decode" in GB/s.
+is timed the same way and reported under "decode" in GB/s, and its grouped-query
+form (32 query heads over 8 K/V heads) under "decode_gqa".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fa|reference]
 
@@ -324,37 +325,46 @@ def run_fa(args, rank, world, local):
     achieved = flops / (ms_mean * 1e-3) / 1e12
     launches = args.steps
 
-    # ---- decode (split-KV + combine)
-    decode = None
-    if not args.no_decode:
-        wd = attn_inputs.WORKLOADS[args.decode_workload]
-        del q, k, v
-        torch.cuda.empty_cache()
+    # ---- decode (split-KV + combine): multi-head, and grouped-query (several query heads per K/V head)
+    def measure_decode(wd, fused=False):
         dq, dk, dv = attn_inputs.make_workload(wd, dev)
         do = torch.empty_like(dq)
         dl = torch.empty((wd.B, wd.H, wd.Nq), dtype=torch.float32, device=dev)
         ws = fa.splitkv_workspace(dq, dk, args.decode_splits)
 
         def dcall():
-            fa.fwd_splitkv(dq, dk, dv, causal=False, scale=wd.scale, num_splits=args.decode_splits, workspace=ws,
-                           out=do, lse=dl)
+            if fused:  # fa_fwd_gqa: a group's query heads as the rows of one tensor-core tile
+                fa.fwd(dq, dk, dv, causal=False, scale=wd.scale, out=do, lse=dl)
+            else:
+                fa.fwd_splitkv(dq, dk, dv, causal=False, scale=wd.scale, num_splits=args.decode_splits,
+                               workspace=ws, out=do, lse=dl)
 
         dms = time_calls(dcall, args.steps, args.warmup, flush)
-        launches += 2 * args.steps
         dmean = statistics.mean(dms)
         dbytes = wd.compulsory_bytes()
         gbs = dbytes / (dmean * 1e-3) / 1e9
         part_bytes = 2 * args.decode_splits * wd.B * wd.H * wd.Nq * (wd.d + 1) * 4
-        decode = {"workload": wd.name, "num_splits": args.decode_splits, "ms_per_call": dmean,
-                  "value": sum_over_ranks(dbytes, world) / (max_over_ranks(dmean, world) * 1e-3) / 1e9,
-                  "unit": "GB/s",
-                  "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                               "frac": gbs / peaks["hbm_gbs"], "traffic": None,
-                               "note": f"compulsory bytes (Q, K, V read, O, LSE written) per call; peak {peak_src}; "
-                                       "split-partial traffic (written and re-read by the combine) excluded: "
-                                       f"{part_bytes} bytes per call"}}
         del dq, dk, dv, ws
         torch.cuda.empty_cache()
+        return {"workload": wd.name, "entry_point": "fa_fwd_gqa" if fused else "fa_fwd_splitkv",
+                "num_splits": None if fused else args.decode_splits, "ms_per_call": dmean,
+                "value": sum_over_ranks(dbytes, world) / (max_over_ranks(dmean, world) * 1e-3) / 1e9,
+                "unit": "GB/s",
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                             "note": f"compulsory bytes (Q, K, V read, O, LSE written) per call; peak {peak_src}"
+                                     + ("" if fused else "; split-partial traffic (written and re-read by the "
+                                        f"combine) excluded: {part_bytes} bytes per call")}}
+
+    decode = decode_gqa = None
+    if not args.no_decode:
+        del q, k, v
+        torch.cuda.empty_cache()
+        decode = measure_decode(attn_inputs.WORKLOADS[args.decode_workload])
+        launches += 2 * args.steps
+        if args.decode_gqa_workload:
+            decode_gqa = measure_decode(attn_inputs.WORKLOADS[args.decode_gqa_workload], fused=True)
+            launches += args.steps
         q, k, v = attn_inputs.make_workload(w, dev)
     sampler.mark(False)
     sampler.stop()
@@ -405,6 +415,7 @@ def run_fa(args, rank, world, local):
                      "peak_source": peak_src,
                      "kernel": "fa_fwd_kernel<128,bf16>", "flops_per_launch": flops},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "decode": decode,
+        "decode_gqa": decode_gqa,
         "wall_s_fwd_timed": wall, "ms_fwd_min": min(ms), "ms_fwd_median": statistics.median(ms),
     }
     if rank == 0:
@@ -440,6 +451,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="b2h32_n8192_d128_bf16_causal", choices=sorted(attn_inputs.WORKLOADS))
     ap.add_argument("--decode-workload", default="decode_b32h32_nk16384_d128_bf16")
     ap.add_argument("--decode-splits", type=int, default=16)
+    ap.add_argument("--decode-gqa-workload", default="decode_b32h32kv8_nk16384_d128_bf16",
+                    help="grouped-query decode workload reported under decode_gqa ('' to skip)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

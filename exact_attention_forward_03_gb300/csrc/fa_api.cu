@@ -137,6 +137,18 @@ int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
     int rc = check_common(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, dtype);
     if (rc != FA_OK) return rc;
     if (H_kv <= 0 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
+    int group = H / H_kv;
+    if (group > 1 && (causal == 0 || Nq == 1) && (long long)group * Nq <= INT32_MAX) {
+        // The `group` query heads of one K/V head are consecutive in q, o and lse, so they
+        // form a single head of group*Nq query rows against that K/V head.  Without a
+        // causal mask (and with one query row, which sees every key) the rows need not
+        // know which head they came from: run that problem, which reads each K/V tile once
+        // for the whole group.
+        H = H_kv;
+        Nq *= group;
+        causal = 0;
+        group = 1;
+    }
     const int num_m = (Nq + kFwdTilesPerCta * kFwdBr - 1) / (kFwdTilesPerCta * kFwdBr);
     if (B * H > 65535) return FA_ERR_INVALID_ARG;  // grid.y limit
     DeviceState *st = nullptr;
@@ -155,7 +167,7 @@ int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
     a.Nk = Nk;
     a.num_m = num_m;
     a.H = H;
-    a.group = H / H_kv;
+    a.group = group;
     a.causal = causal;
     a.scale_log2 = scale * 1.4426950408889634f;
     cudaError_t e = launch_fwd(d, bf16, tq, tk, tv, a, BH, reinterpret_cast<cudaStream_t>(stream));

@@ -7,7 +7,7 @@
 // kernel merges them.  With Nq = 1 every key is read once, so the work is
 // bound by HBM bandwidth; the dot products run on CUDA cores in fp32.
 //
-// Split kernel: one CTA of 128 threads per (split, query row, head).  K/V
+// Split kernel: one CTA of 128 threads per (split, query row, query head).  K/V
 // tiles of 64 keys stream through a 3-stage ring of shared-memory slots,
 // loaded by TMA with the 128-byte swizzle (row r's 16-byte chunk c sits at
 // chunk c ^ (r & 7), so the row-per-thread reads below hit distinct banks).
@@ -60,12 +60,19 @@ __global__ void __launch_bounds__(kSplitThreads)
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
 
+    // CTA order (fastest first): query head within its group, split, query row, K/V
+    // head.  The CTAs of one group that read the same key range are launched side
+    // by side and stream the same K/V tiles at the same time, so under grouped-query
+    // attention all but one of them find the tiles in L2.
     const long long idx = blockIdx.x;
-    const int split = (int)(idx % a.num_splits);
-    const long long rest = idx / a.num_splits;
+    const int hg = (int)(idx % a.group);
+    long long rest = idx / a.group;
+    const int split = (int)(rest % a.num_splits);
+    rest /= a.num_splits;
     const int i = (int)(rest % a.Nq);
-    const int bh = (int)(rest / a.Nq);
-    const int kvh = kv_head(bh, a.H, a.group);  // the K/V head this query head reads
+    const int kvh = (int)(rest / a.Nq);  // K/V head b*H_kv + h_kv
+    const int H_kv = a.H / a.group;
+    const int bh = (kvh / H_kv) * a.H + (kvh % H_kv) * a.group + hg;  // query head b*H + h_kv*group + hg
     const size_t out_row = (size_t)split * a.BH * a.Nq + (size_t)bh * a.Nq + i;
 
     const int k0 = split * a.split_len;

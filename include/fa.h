@@ -141,6 +141,11 @@ FA_API int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, 
  * split-KV workspace is sized by fa_splitkv_workspace_bytes(B, H, ...) as for
  * multi-head attention.  ("Flash Attention (4)" §5: the K/V index mapped per
  * group of query heads; "Lecture 25" §0.3, its table's GQA entry.)
+ * fa_fwd_gqa without causal masking, or with Nq = 1 (decode, where the one
+ * query row sees every key), treats the H/H_kv query heads of a K/V head as
+ * one head of (H/H_kv)*Nq query rows: q, o and lse hold them consecutively, so
+ * the group's rows share each K/V tile on the tensor cores and K/V is read
+ * once per group.
  * Errors: as fa_fwd / fa_fwd_splitkv, plus FA_ERR_INVALID_ARG when H_kv <= 0
  * or H is not a multiple of H_kv.
  */
