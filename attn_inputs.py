@@ -105,6 +105,20 @@ def make_qkv(B: int, H: int, Nq: int, Nk: int, d: int, dtype="f16", seed: int = 
     return q, k, v
 
 
+def varlen_lengths(num_seqs: int, lo: int, hi: int, seed: int) -> list[int]:
+    """Seeded sequence lengths, log-uniform in [lo, hi] (a packed batch of mixed
+    short and long sequences)."""
+    g = torch.Generator().manual_seed(seed)
+    u = torch.rand(num_seqs, generator=g, dtype=torch.float64)
+    return [int(round(math.exp(math.log(lo) + float(x) * (math.log(hi) - math.log(lo))))) for x in u]
+
+
+# Packed variable-length batch: 16 sequences of 256..8192 tokens, 32 heads, d = 128,
+# bf16, causal (q and k have the same lengths).
+VARLEN_WORKLOAD = {"name": "varlen16_l256-8192_h32_d128_bf16_causal", "num_seqs": 16, "lo": 256, "hi": 8192,
+                   "H": 32, "d": 128, "dtype": "bf16", "causal": True, "seed": 7000}
+
+
 def make_workload(w: Workload, device="cpu"):
     if w.kv_heads == w.H:
         return make_qkv(w.B, w.H, w.Nq, w.Nk, w.d, w.dtype, w.seed, device)

@@ -20,6 +20,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import itertools
 import json
 import math
 import os
@@ -356,6 +357,36 @@ def run_fa(args, rank, world, local):
                                      + ("" if fused else "; split-partial traffic (written and re-read by the "
                                         f"combine) excluded: {part_bytes} bytes per call")}}
 
+    # ---- packed variable-length batch (fa_fwd_varlen)
+    varlen = None
+    if not args.no_varlen:
+        vw = attn_inputs.VARLEN_WORKLOAD
+        lens = attn_inputs.varlen_lengths(vw["num_seqs"], vw["lo"], vw["hi"], vw["seed"])
+        total = sum(lens)
+        # packed [total, H, d] tensors: the [B, H, N, d] recipe with B = 1, H = total, N = H
+        vq = attn_inputs.make_qkv(1, total, vw["H"], 1, vw["d"], vw["dtype"], vw["seed"], dev)[0][0]
+        _, vk, vv = attn_inputs.make_qkv(1, total, 1, vw["H"], vw["d"], vw["dtype"], vw["seed"] + 5, dev)
+        vk, vv = vk[0], vv[0]
+        cu = torch.tensor([0] + list(itertools.accumulate(lens)), dtype=torch.int32, device=dev)
+        vo = torch.empty_like(vq)
+        vl = torch.empty((vw["H"], total), dtype=torch.float32, device=dev)
+
+        def vcall():
+            fa.fwd_varlen(vq, vk, vv, cu, cu, max(lens), causal=vw["causal"], out=vo, lse=vl)
+
+        vms = time_calls(vcall, args.steps, args.warmup, flush)
+        launches += args.steps
+        vmean = statistics.mean(vms)
+        vflops = sum(4.0 * vw["H"] * n * n * vw["d"] / (2.0 if vw["causal"] else 1.0) for n in lens)
+        varlen = {"workload": vw["name"], "lengths": lens, "total_tokens": total, "ms_per_call": vmean,
+                  "value": sum_over_ranks(vflops, world) / (max_over_ranks(vmean, world) * 1e-3) / 1e12,
+                  "unit": "TFLOP/s", "flops_per_call": vflops,
+                  "roofline": {"bound": "tensor", "achieved": vflops / (vmean * 1e-3) / 1e12,
+                               "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                               "frac": vflops / (vmean * 1e-3) / 1e12 / peaks["bf16_tflops"], "traffic": None}}
+        del vq, vk, vv, vo, vl
+        torch.cuda.empty_cache()
+
     decode = decode_gqa = None
     if not args.no_decode:
         del q, k, v
@@ -415,7 +446,7 @@ def run_fa(args, rank, world, local):
                      "peak_source": peak_src,
                      "kernel": "fa_fwd_kernel<128,bf16>", "flops_per_launch": flops},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "decode": decode,
-        "decode_gqa": decode_gqa,
+        "decode_gqa": decode_gqa, "varlen": varlen,
         "wall_s_fwd_timed": wall, "ms_fwd_min": min(ms), "ms_fwd_median": statistics.median(ms),
     }
     if rank == 0:
@@ -454,6 +485,7 @@ def main(argv=None):
     ap.add_argument("--decode-gqa-workload", default="decode_b32h32kv8_nk16384_d128_bf16",
                     help="grouped-query decode workload reported under decode_gqa ('' to skip)")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-varlen", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -40,7 +40,7 @@ FA_ERR_SCRATCH_LIMIT = -7
 EXPORTS = ("fa_fwd", "fa_fwd_splitkv", "fa_splitkv_combine", "fa_splitkv_workspace_bytes",
            "fa_splitkv_num_splits", "fa_splitkv_split_len", "fa_get_device_status", "fa_status_string",
            "fa_version", "fa_fwd_splitkv_noalloc", "fa_splitkv_noalloc_capacity_bytes", "fa_fwd_gqa",
-           "fa_fwd_splitkv_gqa")
+           "fa_fwd_splitkv_gqa", "fa_fwd_varlen")
 
 _lock = threading.Lock()
 _lib = None
@@ -87,6 +87,8 @@ def load_library(path: str | None = None):
         lib.fa_fwd_gqa.restype = i
         lib.fa_fwd_splitkv_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, vp, sz, vp]
         lib.fa_fwd_splitkv_gqa.restype = i
+        lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd_varlen.restype = i
         lib.fa_splitkv_noalloc_capacity_bytes.argtypes = []
         lib.fa_splitkv_noalloc_capacity_bytes.restype = sz
         if path is None:
@@ -164,6 +166,45 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
                             int(bool(causal)), scale, _dtype_code(q), _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd" if H_kv == H else "fa_fwd_gqa")
+    return out, lse
+
+
+def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal: bool = False,
+               scale: float | None = None, out=None, lse=None, want_lse: bool = True, stream=None):
+    """Variable-length (packed) batch through ``fa_fwd_varlen``.
+
+    q: [total_q, H, d], k, v: [total_k, H_kv, d] (H_kv divides H), cu_seqlens_q/k:
+    int32 CUDA tensors of num_seqs + 1 offsets.  Returns (o [total_q, H, d],
+    lse [H, total_q]).  ``max_seqlen_q`` must bound every sequence's query length.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or t.dim() != 3 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA [tokens, heads, d] tensor")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if not t.is_cuda or t.dtype != torch.int32 or t.dim() != 1 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA vector")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold num_seqs + 1 offsets")
+    total_q, H, d = q.shape
+    total_k, H_kv = k.shape[0], k.shape[1]
+    if v.shape != k.shape or k.shape[2] != d or H_kv <= 0 or H % H_kv != 0:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must match q")
+    if lse is None and want_lse:
+        lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    lib = load_library()
+    rc = lib.fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           lse.data_ptr() if lse is not None else None, cu_seqlens_q.data_ptr(),
+                           cu_seqlens_k.data_ptr(), cu_seqlens_q.numel() - 1, int(max_seqlen_q), total_q, total_k, H,
+                           H_kv, d, int(bool(causal)), scale, _dtype_code(q), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_varlen")
     return out, lse
 
 

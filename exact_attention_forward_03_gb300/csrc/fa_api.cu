@@ -79,6 +79,21 @@ int make_map(CUtensorMap *map, const void *ptr, bool bf16, int d, int rows, int 
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// Packed [tokens][heads][d] 16-bit tensor of a variable-length batch: boxes of 64
+// columns x 1 head x box_rows tokens (the same 128-byte rows in shared memory as
+// make_map's boxes), 128-byte swizzle; tokens beyond `tokens` read as zero.
+int make_map_packed(CUtensorMap *map, const void *ptr, bool bf16, int d, int heads, int tokens, int box_rows) {
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                          const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int check_common(const void *q, const void *k, const void *v, const void *o, const float *lse, int B, int H,
@@ -168,9 +183,49 @@ int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
     a.num_m = num_m;
     a.H = H;
     a.group = group;
+    a.cu_q = nullptr;
+    a.cu_k = nullptr;
+    a.total_q = 0;
     a.causal = causal;
     a.scale_log2 = scale * 1.4426950408889634f;
     cudaError_t e = launch_fwd(d, bf16, tq, tk, tv, a, BH, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, const int *cu_seqlens_q,
+                  const int *cu_seqlens_k, int num_seqs, int max_seqlen_q, int total_q, int total_k, int H, int H_kv,
+                  int d, int causal, float scale, fa_dtype dtype, fa_stream_t stream) {
+    // The common checks with one "sequence" of the totals stand in for B, Nq, Nk.
+    int rc = check_common(q, k, v, o, lse, 1, H, total_q, total_k, d, causal, scale, dtype);
+    if (rc != FA_OK) return rc;
+    if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return FA_ERR_INVALID_ARG;
+    if (!aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4)) return FA_ERR_MISALIGNED;
+    if (num_seqs <= 0 || max_seqlen_q <= 0 || max_seqlen_q > total_q) return FA_ERR_INVALID_ARG;
+    if (H_kv <= 0 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
+    if ((long long)num_seqs * H > 65535) return FA_ERR_INVALID_ARG;  // grid.y limit
+    DeviceState *st = nullptr;
+    if ((rc = dev_state(&st)) != FA_OK) return rc;
+    const bool bf16 = dtype == FA_BF16;
+    CUtensorMap tq, tk, tv;
+    if (make_map_packed(&tq, q, bf16, d, H, total_q, kFwdBr) != FA_OK ||
+        make_map_packed(&tk, k, bf16, d, H_kv, total_k, kFwdBc) != FA_OK ||
+        make_map_packed(&tv, v, bf16, d, H_kv, total_k, kFwdBc) != FA_OK)
+        return FA_ERR_CUDA;
+    FwdArgs a;
+    a.o = o;
+    a.lse = lse;
+    a.status = st->status;
+    a.Nq = 0;
+    a.Nk = 0;
+    a.num_m = (max_seqlen_q + kFwdBr - 1) / kFwdBr;
+    a.H = H;
+    a.group = H / H_kv;
+    a.cu_q = cu_seqlens_q;
+    a.cu_k = cu_seqlens_k;
+    a.total_q = total_q;
+    a.causal = causal;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    cudaError_t e = launch_fwd_varlen(d, bf16, tq, tk, tv, a, num_seqs, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -238,7 +238,13 @@ __device__ __noinline__ void rescale_o(uint32_t o_addr, float alpha) {
     }
 }
 
-template <int D, bool BF16>
+// VARLEN: packed variable-length batch.  blockIdx.y = sequence * H + head, q, o
+// are [total_q, H, d], k, v are [total_k, H_kv, d] (tensor maps indexed by column,
+// head, token), lse is [H, total_q], and sequence s spans tokens
+// [cu_q[s], cu_q[s+1]) of q and [cu_k[s], cu_k[s+1]) of k and v.  A key tile may
+// run past its sequence's last key into the next sequence: those keys are masked
+// like the ragged tail of a dense K.  Query rows past the sequence are not stored.
+template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
@@ -255,9 +261,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // Consecutive CTAs take consecutive row blocks of one head, heaviest causal
     // block first, so the CTAs resident at any time share a few heads' K/V in L2.
     const int bh = blockIdx.y;
-    const int q0 = (args.num_m - 1 - (int)blockIdx.x) * kFwdBr;
-    const int Nq = args.Nq, Nk = args.Nk, causal = args.causal;
-    const int kvh = kv_head(bh, args.H, args.group);  // the K/V head this query head reads
+    const int causal = args.causal;
+    int q0, Nq, Nk, kvh;
+    int q_tok = 0, k_tok = 0;  // VARLEN: first token of this sequence in q and in k, v
+    if constexpr (VARLEN) {
+        const int seq = bh / args.H;
+        q_tok = args.cu_q[seq];
+        k_tok = args.cu_k[seq];
+        Nq = args.cu_q[seq + 1] - q_tok;
+        Nk = args.cu_k[seq + 1] - k_tok;
+        const int num_m = (Nq + kFwdBr - 1) / kFwdBr;
+        // Row blocks past this sequence's own ones hold no row: q0 >= Nq gives n = 0.
+        q0 = (int)blockIdx.x < num_m ? (num_m - 1 - (int)blockIdx.x) * kFwdBr : max(Nq, 0);
+        kvh = (bh % args.H) / args.group;  // K/V head index within the token's heads
+    } else {
+        q0 = (args.num_m - 1 - (int)blockIdx.x) * kFwdBr;
+        Nq = args.Nq;
+        Nk = args.Nk;
+        kvh = kv_head(bh, args.H, args.group);  // the K/V head this query head reads
+    }
+    // A variable-length grid is sized by the longest sequence: a CTA past its own
+    // sequence's row blocks holds no row and leaves before touching shared or tensor
+    // memory (the whole CTA takes this branch together).
+    if (VARLEN && q0 >= Nq) return;
     const int n = fwd_tile_count(q0, Nq, Nk, causal);
     const int jm = fwd_first_masked_tile(q0, Nq, Nk, causal);
 
@@ -317,7 +343,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             uint32_t par_k = 0, par_v = 0;    // phase parity of the last load into each slot
             mbar_arrive_expect_tx(bar(B_QFULL), C::kQBytes);
             for (int b = 0; b < C::kBlocks; ++b)
-                tma_load_3d(sb + C::kOffQ + b * C::kQBlockBytes, &tmQ, b * 64, q0, bh, bar(B_QFULL));
+                if constexpr (VARLEN)
+                    tma_load_3d(sb + C::kOffQ + b * C::kQBlockBytes, &tmQ, b * 64, bh % args.H, q_tok + q0, bar(B_QFULL));
+                else
+                    tma_load_3d(sb + C::kOffQ + b * C::kQBlockBytes, &tmQ, b * 64, q0, bh, bar(B_QFULL));
             // Tile `tile` of K (V) goes to slot tile % S of its ring, in the order the two
             // MMA streams consume them: K_0, K_1, K_2, then V_j, K_{j+3} for j = 0, 1, ...
             auto load = [&](bool is_v, int tile) -> bool {
@@ -329,7 +358,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 mbar_arrive_expect_tx(full, C::kTileBytes);
                 const uint32_t dst = sb + (is_v ? C::kOffV : C::kOffK) + s * C::kTileBytes;
                 for (int b = 0; b < C::kBlocks; ++b)
-                    tma_load_3d(dst + b * C::kKVBlockBytes, is_v ? &tmV : &tmK, b * 64, tile * kFwdBc, kvh, full);
+                    if constexpr (VARLEN)
+                        tma_load_3d(dst + b * C::kKVBlockBytes, is_v ? &tmV : &tmK, b * 64, kvh, k_tok + tile * kFwdBc, full);
+                    else
+                        tma_load_3d(dst + b * C::kKVBlockBytes, is_v ? &tmV : &tmK, b * 64, tile * kFwdBc, kvh, full);
                 (is_v ? pend_v : pend_k) |= 1u << s;
                 uint32_t &par = is_v ? par_v : par_k;
                 par = (par & ~(1u << s)) | ((it & 1u) << s);
@@ -455,7 +487,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             // Epilogue: O = O~ / l (0 for a row that saw no key), LSE = m ln2 + ln l.
             const bool valid = i < Nq;
             const float inv = (l > 0.f) ? 1.f / l : 0.f;
-            typename PK::T *orow_g = reinterpret_cast<typename PK::T *>(args.o) + ((size_t)bh * Nq + i) * D;
+            const size_t orow = VARLEN ? (size_t)(q_tok + i) * args.H + bh % args.H : (size_t)bh * Nq + i;
+            typename PK::T *orow_g = reinterpret_cast<typename PK::T *>(args.o) + orow * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t ov[32];
@@ -478,7 +511,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             }
             if (valid && args.lse != nullptr) {
                 const float m_fin = (m == -INFINITY) ? 0.f : m;
-                args.lse[(size_t)bh * Nq + i] = (l > 0.f) ? m_fin * 0.69314718055994531f + logf(l) : -INFINITY;
+                const size_t lrow = VARLEN ? (size_t)(bh % args.H) * args.total_q + q_tok + i : (size_t)bh * Nq + i;
+                args.lse[lrow] = (l > 0.f) ? m_fin * 0.69314718055994531f + logf(l) : -INFINITY;
             }
         }
     }
@@ -492,24 +526,35 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool VARLEN>
 static cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                                const FwdArgs &a, int BH, cudaStream_t stream) {
+                                const FwdArgs &a, int num_m, int rows_y, cudaStream_t stream) {
     using C = FwdCfg<D>;
-    auto kern = fa_fwd_kernel<D, BF16>;
+    auto kern = fa_fwd_kernel<D, BF16, VARLEN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)a.num_m, (unsigned)BH, 1);
+    dim3 grid((unsigned)num_m, (unsigned)rows_y, 1);
     kern<<<grid, kFwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
     return cudaGetLastError();
 }
 
+template <bool VARLEN>
+static cudaError_t launch_fwd_any(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
+                                  const CUtensorMap &tv, const FwdArgs &a, int rows_y, cudaStream_t stream) {
+    if (d == 64) return bf16 ? launch_fwd_t<64, true, VARLEN>(tq, tk, tv, a, a.num_m, rows_y, stream)
+                             : launch_fwd_t<64, false, VARLEN>(tq, tk, tv, a, a.num_m, rows_y, stream);
+    return bf16 ? launch_fwd_t<128, true, VARLEN>(tq, tk, tv, a, a.num_m, rows_y, stream)
+                : launch_fwd_t<128, false, VARLEN>(tq, tk, tv, a, a.num_m, rows_y, stream);
+}
+
 cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdArgs &a, int BH, cudaStream_t stream) {
-    if (d == 64) return bf16 ? launch_fwd_t<64, true>(tq, tk, tv, a, BH, stream)
-                             : launch_fwd_t<64, false>(tq, tk, tv, a, BH, stream);
-    return bf16 ? launch_fwd_t<128, true>(tq, tk, tv, a, BH, stream)
-                : launch_fwd_t<128, false>(tq, tk, tv, a, BH, stream);
+    return launch_fwd_any<false>(d, bf16, tq, tk, tv, a, BH, stream);
+}
+
+cudaError_t launch_fwd_varlen(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                              const FwdArgs &a, int num_seqs, cudaStream_t stream) {
+    return launch_fwd_any<true>(d, bf16, tq, tk, tv, a, num_seqs * a.H, stream);
 }
 
 }  // namespace fa

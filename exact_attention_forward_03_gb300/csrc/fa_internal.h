@@ -28,6 +28,11 @@ struct FwdArgs {
     int num_m;      // ceil(Nq / (kFwdTilesPerCta * kFwdBr)): row blocks per head
     int H;          // query heads per batch entry
     int group;      // query heads per K/V head (H / H_kv)
+    // Variable-length batches (packed [total, heads, d] tensors): per-sequence token
+    // offsets, cu_q[s]..cu_q[s+1] and cu_k[s]..cu_k[s+1]; null for dense [B, H, N, d].
+    const int *cu_q;
+    const int *cu_k;
+    int total_q;    // tokens in the packed q (the lse layout is [H, total_q])
     int causal;
     float scale_log2;  // scale * log2(e)
 };
@@ -56,6 +61,10 @@ struct CombineArgs {
 // Each launcher returns the CUDA error of the launch (cudaSuccess when queued).
 cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdArgs &a, int BH, cudaStream_t stream);
+// Variable-length form: grid (num_m, num_seqs * H), packed tensor maps (x = column,
+// y = head, z = token), a.cu_q / a.cu_k set.
+cudaError_t launch_fwd_varlen(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                              const FwdArgs &a, int num_seqs, cudaStream_t stream);
 cudaError_t launch_splitkv(int d, bool bf16, const CUtensorMap &tk, const CUtensorMap &tv, const SplitArgs &a,
                            cudaStream_t stream);
 cudaError_t launch_combine(int d, bool bf16, const CombineArgs &a, cudaStream_t stream);

@@ -149,6 +149,33 @@ FA_API int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, 
  * Errors: as fa_fwd / fa_fwd_splitkv, plus FA_ERR_INVALID_ARG when H_kv <= 0
  * or H is not a multiple of H_kv.
  */
+/*
+ * Variable-length batch (packed sequences): num_seqs sequences of different
+ * lengths in one launch, each attending only within itself.  q, o are packed
+ * [total_q, H, d] and k, v [total_k, H_kv, d] (token-major, contiguous, 16-bit);
+ * lse is [H, total_q] fp32 or NULL.  cu_seqlens_q and cu_seqlens_k are DEVICE
+ * arrays of num_seqs + 1 int32 offsets: sequence s owns query tokens
+ * [cu_seqlens_q[s], cu_seqlens_q[s+1]) and keys [cu_seqlens_k[s], cu_seqlens_k[s+1]).
+ * Per sequence this is fa_fwd_gqa with Nq = its query length, Nk = its key
+ * length (the causal diagonal aligned to its bottom-right corner); a sequence
+ * with no key gets O = 0 and LSE = -inf.  The caller guarantees
+ * 0 = cu[0] <= cu[1] <= ... <= cu[num_seqs] = total for both arrays and that no
+ * sequence has more than max_seqlen_q query tokens (the grid is sized by it);
+ * the offsets are read on the device only.  A key tile may extend past its
+ * sequence into the next one; those keys get weight exactly 0, so K and V must
+ * be finite everywhere (0 * inf is NaN).  ("Flash Attention (4)" §5: an entry
+ * with cu_seqlens; "Lecture 25" §7.1 item 07 and §7.2 item 2: sequence packing
+ * without padding.)
+ * Errors: the common ones (with total_q, total_k in the places of Nq, Nk), and
+ * FA_ERR_INVALID_ARG for null offsets, num_seqs <= 0, max_seqlen_q outside
+ * [1, total_q], H not a multiple of H_kv, or num_seqs * H > 65535;
+ * FA_ERR_MISALIGNED for offsets not 4-byte aligned.
+ */
+FA_API int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+           const int *cu_seqlens_q, const int *cu_seqlens_k, int num_seqs, int max_seqlen_q,
+           int total_q, int total_k, int H, int H_kv, int d, int causal, float scale,
+           fa_dtype dtype, fa_stream_t stream);
+
 FA_API int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
            int B, int H, int H_kv, int Nq, int Nk, int d, int causal, float scale,
            fa_dtype dtype, fa_stream_t stream);

@@ -214,6 +214,31 @@ def attention_gqa(q, k, v, causal: bool, scale: float, lib=None):
     return o.reshape(B, H, Nq, d), lse.reshape(B, H, Nq)
 
 
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool, scale: float, lib=None):
+    """Exact attention of a packed variable-length batch.  q: [total_q, H, d], k, v:
+    [total_k, H_kv, d], cu_seqlens_q/k: num_seqs + 1 token offsets.  Sequence s is
+    its own problem (attention_gqa on tokens [cu_q[s], cu_q[s+1]) of q and
+    [cu_k[s], cu_k[s+1]) of k and v, causal diagonal at its bottom-right corner);
+    a row with no key gets O = 0, LSE = -inf.  Returns (O [total_q, H, d], LSE [H, total_q])."""
+    q64, k64, v64 = to_f64(q), to_f64(k), to_f64(v)
+    cq = [int(x) for x in np.asarray(to_f64(cu_seqlens_q))]
+    ck = [int(x) for x in np.asarray(to_f64(cu_seqlens_k))]
+    total_q, H, d = q64.shape
+    o = np.zeros_like(q64)
+    lse = np.full((H, total_q), -np.inf)
+    for s in range(len(cq) - 1):
+        q_s = q64[cq[s]:cq[s + 1]]
+        k_s, v_s = k64[ck[s]:ck[s + 1]], v64[ck[s]:ck[s + 1]]
+        if q_s.shape[0] == 0 or k_s.shape[0] == 0:
+            continue  # no rows, or rows that see no key (O = 0, LSE = -inf)
+        o_s, l_s = attention_gqa(np.ascontiguousarray(q_s.transpose(1, 0, 2))[None],
+                                 np.ascontiguousarray(k_s.transpose(1, 0, 2))[None],
+                                 np.ascontiguousarray(v_s.transpose(1, 0, 2))[None], causal, scale, lib=lib)
+        o[cq[s]:cq[s + 1]] = o_s[0].transpose(1, 0, 2)
+        lse[:, cq[s]:cq[s + 1]] = l_s[0]
+    return o, lse
+
+
 def sampled_rows(q, k, v, pairs, causal: bool, scale: float, heads_per_batch: int = 16):
     """Oracle values for the (bh, row) pairs of ``[B, H, N, d]`` tensors (any device).
 
