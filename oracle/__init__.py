@@ -56,6 +56,9 @@ def _bind(lib):
     lib.oracle_attn_full.argtypes = [_dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_double, _dp, _dp]
     lib.oracle_attn_full.restype = ctypes.c_int
+    lib.oracle_attn_bwd.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_double, _dp, _dp, _dp]
+    lib.oracle_attn_bwd.restype = ctypes.c_int
     lib.oracle_attn_rows.argtypes = [_dp, _i64p, _i64p, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_int, ctypes.c_double, _dp, _dp]
     lib.oracle_attn_rows.restype = ctypes.c_int
@@ -121,6 +124,25 @@ def attention(q, k, v, causal: bool, scale: float, lib=None):
     if rc != 0:
         raise ValueError(f"oracle_attn_full failed ({rc})")
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, causal: bool, scale: float, lib=None):
+    """Gradients (dQ, dK, dV) of O = softmax(scale * Q K^T + mask) V for the given dO
+    ("Lecture 25" §3.3).  q, dout: [..., Nq, d]; k, v: [..., Nk, d]."""
+    lib = lib or load()
+    q, k, v, dout = to_f64(q), to_f64(k), to_f64(v), to_f64(dout)
+    lead = q.shape[:-2]
+    Nq, d = q.shape[-2:]
+    Nk = k.shape[-2]
+    BH = int(np.prod(lead)) if lead else 1
+    dq = np.zeros(q.shape, dtype=np.float64)
+    dk = np.zeros(k.shape, dtype=np.float64)
+    dv = np.zeros(v.shape, dtype=np.float64)
+    rc = lib.oracle_attn_bwd(_p(q), _p(k), _p(v), _p(dout), BH, Nq, Nk, d, int(bool(causal)), float(scale),
+                             _p(dq), _p(dk), _p(dv))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_bwd failed ({rc})")
+    return dq, dk, dv
 
 
 def attention_tiled(q, k, v, causal: bool, scale: float, Br: int, Bc: int, lib=None):

@@ -31,6 +31,9 @@
  *    (4) v2.1 forward", §3.5) guards l == 0 by using 1 instead of 1/l, which
  *    leaves the zero accumulator as the output.
  *
+ * The backward (oracle_attn_bwd, at the end of this file) is the chain rule of
+ * this definition.
+ *
  * Two further modes exist only to check invariants of the method:
  *  - oracle_attn_tiled: the page-4 §6 online-softmax loop in fp64, over KV
  *    tiles of a caller-chosen width (with page 1 §2.5's rule that a running
@@ -328,4 +331,75 @@ int oracle_combine(const double *o_part, const double *lse_part, int num_splits,
         lse[r] = M + log(wsum);
     }
     return 0;
+}
+
+/*
+ * Backward of the definition: the gradients of O = softmax(scale * Q K^T + mask) V
+ * with respect to Q, K and V, given dO (the gradient of a loss with respect to O).
+ *
+ *   P     = softmax(scale * Q K^T + mask)        (the forward's row-normalised weights)
+ *   dV    = P^T dO
+ *   dP    = dO V^T
+ *   dS    = P o (dP - rowsum(dP o P))            (o: elementwise product)
+ *   dQ    = scale * dS K,     dK = scale * dS^T Q
+ *
+ * ("Lecture 25" §3.3, the backward's chain-rule formulas, with P recomputed from
+ * the scores rather than stored; the factor `scale` is the chain rule through
+ * S = scale * Q K^T, which the page's formulas leave out because they write S
+ * with the scale folded in.)  A row that sees no key has P = 0 and contributes
+ * nothing.  Heads are independent and may run on several OpenMP threads; within
+ * a head the rows are taken in order, so dK and dV are plain sums.
+ * q, dout, dq: [BH][Nq][d]; k, v, dk, dv: [BH][Nk][d]; fp64, contiguous.
+ */
+int oracle_attn_bwd(const double *q, const double *k, const double *v, const double *dout,
+                    int BH, int Nq, int Nk, int d, int causal, double scale,
+                    double *dq, double *dk, double *dv) {
+    if (BH < 0 || Nq < 0 || Nk < 0 || d <= 0) return -1;
+    int bad = 0;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(g_threads) reduction(| : bad)
+#endif
+    for (int h = 0; h < BH; ++h) {
+        const double *qh = q + (size_t)h * Nq * d, *kh = k + (size_t)h * Nk * d, *vh = v + (size_t)h * Nk * d;
+        const double *doh = dout + (size_t)h * Nq * d;
+        double *dqh = dq + (size_t)h * Nq * d, *dkh = dk + (size_t)h * Nk * d, *dvh = dv + (size_t)h * Nk * d;
+        memset(dqh, 0, sizeof(double) * (size_t)Nq * d);
+        memset(dkh, 0, sizeof(double) * (size_t)Nk * d);
+        memset(dvh, 0, sizeof(double) * (size_t)Nk * d);
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1) * 3 + sizeof(double) * d);
+        if (s == NULL) { bad = 1; continue; }
+        double *p = s + (Nk > 0 ? Nk : 1), *dp = p + (Nk > 0 ? Nk : 1), *orow = dp + (Nk > 0 ? Nk : 1);
+        for (long i = 0; i < Nq; ++i) {
+            const double *qi = qh + (size_t)i * d, *doi = doh + (size_t)i * d;
+            double lse;
+            const double l = attn_row_range(qi, kh, vh, i, Nq, Nk, d, causal, scale, 0, Nk, s, p, orow, &lse);
+            if (l == 0.0) continue; /* no visible key: P = 0 */
+            /* P row normalised; dP = dO_i . v_j; D = rowsum(dP o P) */
+            double D = 0.0;
+            for (long j = 0; j < Nk; ++j) {
+                p[j] /= l;
+                double acc = 0.0;
+                if (p[j] != 0.0) {
+                    const double *vj = vh + (size_t)j * d;
+                    for (int t = 0; t < d; ++t) acc += doi[t] * vj[t];
+                }
+                dp[j] = acc;
+                D += p[j] * acc;
+            }
+            double *dqi = dqh + (size_t)i * d;
+            for (long j = 0; j < Nk; ++j) {
+                if (p[j] == 0.0) continue;
+                const double ds = p[j] * (dp[j] - D);
+                const double *kj = kh + (size_t)j * d;
+                double *dkj = dkh + (size_t)j * d, *dvj = dvh + (size_t)j * d;
+                for (int t = 0; t < d; ++t) {
+                    dvj[t] += p[j] * doi[t];
+                    dqi[t] += scale * ds * kj[t];
+                    dkj[t] += scale * ds * qi[t];
+                }
+            }
+        }
+        free(s);
+    }
+    return bad ? -2 : 0;
 }

@@ -3,7 +3,7 @@
 Each ``pin_*`` function takes a loaded oracle library and raises
 ``AssertionError`` when the oracle disagrees with a closed form, an invariant
 of the method, brute force on a tiny input, or an independent library routine
-(torch's CPU scaled_dot_product_attention / logsumexp in fp64).  The same
+(torch's CPU scaled_dot_product_attention / logsumexp / autograd in fp64).  The same
 functions run against deliberately broken copies of the oracle in
 ``test_oracle_mutants.py`` to show that the pins catch plausible mistakes.
 """
@@ -270,6 +270,104 @@ def pin_rows_matches_full(lib):
     for n, (bh, r) in enumerate(pairs):
         assert np.allclose(orow[n], o[bh, r], atol=0, rtol=0)
         assert lrow[n] == lse[bh, r]
+
+
+def _loss_grad_fd(q, k, v, g, causal, scale, lib, h=1e-6):
+    """Central differences of L = sum(O * g) with respect to every entry of q, k and v."""
+    out = []
+    for x in (q, k, v):
+        dx = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = x[idx]
+            x[idx] = old + h
+            op, _ = oracle.attention(q, k, v, causal, scale, lib=lib)
+            x[idx] = old - h
+            om, _ = oracle.attention(q, k, v, causal, scale, lib=lib)
+            x[idx] = old
+            dx[idx] = ((op - om) * g).sum() / (2 * h)
+        out.append(dx)
+    return out
+
+
+def pin_bwd_finite_differences(lib):
+    """The backward is the derivative of the forward: central differences of
+    L = sum(O * dO) through the forward definition ("Lecture 25" §3.3).
+
+    The cases include Nq != Nk and, causal with Nq > Nk, rows that see no key."""
+    for n, (Nq, Nk, d, causal) in enumerate([(4, 6, 3, False), (5, 5, 2, True), (6, 3, 2, True)]):
+        q = _rand((1, Nq, d), 40 + n)
+        k = _rand((1, Nk, d), 50 + n)
+        v = _rand((1, Nk, d), 60 + n)
+        g = _rand((1, Nq, d), 70 + n)
+        dq, dk, dv = oracle.attention_bwd(q, k, v, g, causal, 0.7, lib=lib)
+        fq, fk, fv = _loss_grad_fd(q, k, v, g, causal, 0.7, lib)
+        for got, want in ((dq, fq), (dk, fk), (dv, fv)):
+            assert np.allclose(got, want, atol=1e-8, rtol=0), n
+
+
+def pin_bwd_two_key_closed_form(lib):
+    """d = 1, one query, two keys: O = w v0 + (1 - w) v1 with w = sigmoid(a),
+    a = scale q (k0 - k1).  With dO = g: dv0 = w g, dv1 = (1 - w) g,
+    dq = w(1-w) scale (k0 - k1)(v0 - v1) g, dk0 = -dk1 = w(1-w) scale q (v0 - v1) g."""
+    for (qv, k0, k1, v0, v1, g, sc) in [(0.8, 0.5, -1.0, 2.0, -1.0, 1.5, 0.9), (-1.2, 2.0, 0.3, 0.5, 3.0, -0.7, 1.3)]:
+        q = np.array([[[qv]]])
+        k = np.array([[[k0], [k1]]])
+        v = np.array([[[v0], [v1]]])
+        dq, dk, dv = oracle.attention_bwd(q, k, v, np.array([[[g]]]), False, sc, lib=lib)
+        w = 1.0 / (1.0 + math.exp(-sc * qv * (k0 - k1)))
+        ww = w * (1.0 - w)
+        assert abs(dv[0, 0, 0] - w * g) < TOL and abs(dv[0, 1, 0] - (1 - w) * g) < TOL
+        assert abs(dq[0, 0, 0] - ww * sc * (k0 - k1) * (v0 - v1) * g) < TOL
+        assert abs(dk[0, 0, 0] - ww * sc * qv * (v0 - v1) * g) < TOL
+        assert abs(dk[0, 1, 0] + ww * sc * qv * (v0 - v1) * g) < TOL
+
+
+def pin_bwd_autograd_library(lib):
+    """Independent library routine: torch autograd in fp64 through CPU
+    scaled_dot_product_attention (square and bottom-right causal)."""
+    cases = [(1, 2, 40, 40, 16, True), (2, 1, 33, 70, 8, False), (1, 1, 20, 50, 32, True), (1, 2, 64, 64, 64, False)]
+    for n, (B, H, Nq, Nk, d, causal) in enumerate(cases):
+        gen = torch.Generator().manual_seed(200 + n)
+        q = torch.randn(B, H, Nq, d, generator=gen, dtype=torch.float64, requires_grad=True)
+        k = torch.randn(B, H, Nk, d, generator=gen, dtype=torch.float64, requires_grad=True)
+        v = torch.randn(B, H, Nk, d, generator=gen, dtype=torch.float64, requires_grad=True)
+        g = torch.randn(B, H, Nq, d, generator=gen, dtype=torch.float64)
+        scale = 1.0 / math.sqrt(d)
+        mask = None
+        if causal:
+            mask = torch.arange(Nk)[None, :] <= torch.arange(Nq)[:, None] + (Nk - Nq)
+        o = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale)
+        o.backward(g)
+        dq, dk, dv = oracle.attention_bwd(q.detach(), k.detach(), v.detach(), g, causal, scale, lib=lib)
+        for got, want in ((dq, q.grad), (dk, k.grad), (dv, v.grad)):
+            assert np.allclose(got, want.numpy(), atol=1e-11, rtol=0), f"case {n}"
+
+
+def pin_bwd_invariants(lib):
+    """Facts of the gradient that hold at any size.
+
+    Adding one vector to every key leaves every softmax row unchanged, so the
+    dK rows of a head sum to zero; rows of P sum to one, so the dV rows sum to
+    the dO rows of the rows that see a key; a row that sees no key has dQ = 0;
+    the gradient is linear in dO."""
+    BH, Nq, Nk, d = 2, 9, 5, 4
+    q = _rand((BH, Nq, d), 80)
+    k = _rand((BH, Nk, d), 81)
+    v = _rand((BH, Nk, d), 82)
+    g1 = _rand((BH, Nq, d), 83)
+    g2 = _rand((BH, Nq, d), 84)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, g1, True, 0.6, lib=lib)
+    assert np.allclose(dk.sum(axis=1), 0.0, atol=1e-12, rtol=0)
+    seen = Nq - Nk  # causal, Nq > Nk: rows below this index see no key
+    assert np.allclose(dv.sum(axis=1), g1[:, seen:].sum(axis=1), atol=1e-12, rtol=0)
+    assert (dq[:, :seen] == 0).all() and np.abs(dq[:, seen:]).max() > 0
+    a = oracle.attention_bwd(q, k, v, g1, True, 0.6, lib=lib)
+    b = oracle.attention_bwd(q, k, v, g2, True, 0.6, lib=lib)
+    c = oracle.attention_bwd(q, k, v, 2.0 * g1 - 3.0 * g2, True, 0.6, lib=lib)
+    for x, y, z in zip(a, b, c):
+        assert np.allclose(z, 2.0 * x - 3.0 * y, atol=1e-12, rtol=0)
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -24,6 +24,11 @@ MUTANTS = {
     "combine_weight_sign": ("double w = (ls == -INFINITY) ? 0.0 : exp(ls - M);",
                             "double w = (ls == -INFINITY) ? 0.0 : exp(M - ls);"),
     "combine_lse_no_max": ("lse[r] = M + log(wsum);", "lse[r] = log(wsum);"),
+    "bwd_drop_rowsum_term": ("const double ds = p[j] * (dp[j] - D);", "const double ds = p[j] * dp[j];"),
+    "bwd_dq_without_scale": ("dqi[t] += scale * ds * kj[t];", "dqi[t] += ds * kj[t];"),
+    "bwd_dk_from_keys": ("dkj[t] += scale * ds * qi[t];", "dkj[t] += scale * ds * kj[t];"),
+    "bwd_dv_unnormalised": ("p[j] /= l;", ""),
+    "bwd_dp_against_keys": ("const double *vj = vh + (size_t)j * d;", "const double *vj = kh + (size_t)j * d;"),
     "exp_without_shift_guard": ("double m_sub = (m_new == -INFINITY) ? 0.0 : m_new;", "double m_sub = m_new;"),
 }
 
