@@ -105,6 +105,12 @@ def make_qkv(B: int, H: int, Nq: int, Nk: int, d: int, dtype="f16", seed: int = 
     return q, k, v
 
 
+def make_dout(B: int, H: int, Nq: int, d: int, dtype="f16", seed: int = 0, device="cpu"):
+    """Draw the output gradient dO [B, H, Nq, d] with the same recipe (standard normal)."""
+    tdt = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    return _randn((B, H, Nq, d), tdt, seed + 4, device)
+
+
 def varlen_lengths(num_seqs: int, lo: int, hi: int, seed: int) -> list[int]:
     """Seeded sequence lengths, log-uniform in [lo, hi] (a packed batch of mixed
     short and long sequences)."""

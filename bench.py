@@ -8,7 +8,8 @@ causal, timed with CUDA events around every fa_fwd launch on the launching
 stream, with the L2 cache flushed (a 256 MiB write) before each timed launch.
 The split-KV decode path (B=32, H=32, Nq=1, Nk=16384, d=128, bf16, 16 splits)
 is timed the same way and reported under "decode" in GB/s, and its grouped-query
-form (32 query heads over 8 K/V heads) under "decode_gqa".
+form (32 query heads over 8 K/V heads) under "decode_gqa".  The backward of the
+default workload (fa_bwd, 2.5x the forward's FLOPs) is reported under "bwd".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fa|reference]
 
@@ -387,6 +388,33 @@ def run_fa(args, rank, world, local):
         del vq, vk, vv, vo, vl
         torch.cuda.empty_cache()
 
+    # ---- backward (fa_bwd: preprocess, main K/V-block kernel, dQ conversion) on the same workload
+    bwd = None
+    if not args.no_bwd:
+        gout = attn_inputs.make_dout(w.B, w.H, w.Nq, w.d, w.dtype, w.seed, dev)
+        fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse)
+        gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        gws = torch.empty(fa.bwd_workspace_bytes(w.B, w.H, w.Nq, w.d), dtype=torch.uint8, device=dev)
+
+        def bcall():
+            fa.bwd(q, k, v, o, gout, lse, causal=w.causal, scale=w.scale, dq=gq, dk=gk, dv=gv, workspace=gws)
+
+        bms = time_calls(bcall, args.steps, args.warmup, flush)
+        launches += 3 * args.steps
+        bmean = statistics.mean(bms)
+        bflops = 2.5 * flops  # five products of the forward's size against the forward's two
+        bwd = {"workload": w.name, "entry_point": "fa_bwd", "launches_per_call": 3, "ms_per_call": bmean,
+               "ms_min": min(bms), "value": sum_over_ranks(bflops, world) / (max_over_ranks(bmean, world) * 1e-3) / 1e12,
+               "unit": "TFLOP/s", "flops_per_call": bflops,
+               "roofline": {"bound": "tensor", "achieved": bflops / (bmean * 1e-3) / 1e12, "peak": peaks["bf16_tflops"],
+                            "unit": "TFLOP/s", "frac": bflops / (bmean * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                            "traffic": None, "note": "whole call (three launches) timed; FLOPs 2.5x the forward's"}}
+        status = fa.get_device_status()
+        if status != fa.FA_OK:
+            raise RuntimeError(f"device status {status} after the backward")
+        del gout, gq, gk, gv, gws
+        torch.cuda.empty_cache()
+
     decode = decode_gqa = None
     if not args.no_decode:
         del q, k, v
@@ -446,7 +474,7 @@ def run_fa(args, rank, world, local):
                      "peak_source": peak_src,
                      "kernel": "fa_fwd_kernel<128,bf16>", "flops_per_launch": flops},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "decode": decode,
-        "decode_gqa": decode_gqa, "varlen": varlen,
+        "decode_gqa": decode_gqa, "varlen": varlen, "bwd": bwd,
         "wall_s_fwd_timed": wall, "ms_fwd_min": min(ms), "ms_fwd_median": statistics.median(ms),
     }
     if rank == 0:
@@ -486,6 +514,7 @@ def main(argv=None):
                     help="grouped-query decode workload reported under decode_gqa ('' to skip)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-varlen", action="store_true")
+    ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

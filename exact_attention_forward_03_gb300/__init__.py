@@ -10,7 +10,9 @@ Functions (same names as the C ABI without the ``fa_`` prefix):
     fwd(q, k, v, causal=False, scale=None, out=None, lse=None)            -> (o, lse)
     fwd_splitkv(q, k, v, causal=False, scale=None, num_splits=0, ...)     -> (o, lse)
     splitkv_combine(o_part, lse_part, out=None, lse=None, dtype=...)      -> (o, lse)
-    splitkv_num_splits, splitkv_split_len, splitkv_workspace_bytes,
+    bwd(q, k, v, o, dout, lse, causal=False, scale=None, ...)            -> (dq, dk, dv)
+    attention(q, k, v, causal=False, scale=None)   differentiable: fwd, then bwd in backward
+    splitkv_num_splits, splitkv_split_len, splitkv_workspace_bytes, bwd_workspace_bytes,
     get_device_status, status_string, version
 Tensors are ``[B, H, N, d]`` contiguous fp16 or bf16 on one CUDA device;
 ``lse`` is ``[B, H, Nq]`` fp32.
@@ -40,7 +42,7 @@ FA_ERR_SCRATCH_LIMIT = -7
 EXPORTS = ("fa_fwd", "fa_fwd_splitkv", "fa_splitkv_combine", "fa_splitkv_workspace_bytes",
            "fa_splitkv_num_splits", "fa_splitkv_split_len", "fa_get_device_status", "fa_status_string",
            "fa_version", "fa_fwd_splitkv_noalloc", "fa_splitkv_noalloc_capacity_bytes", "fa_fwd_gqa",
-           "fa_fwd_splitkv_gqa", "fa_fwd_varlen")
+           "fa_fwd_splitkv_gqa", "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace_bytes", "fa_last_error")
 
 _lock = threading.Lock()
 _lib = None
@@ -48,7 +50,13 @@ _lib = None
 
 class FaError(RuntimeError):
     def __init__(self, code: int, what: str):
-        super().__init__(f"{what}: {status_string(code)} ({code})")
+        detail = ""
+        if code == FA_ERR_CUDA:
+            try:
+                detail = " [" + load_library().fa_last_error().decode() + "]"
+            except RuntimeError:
+                pass
+        super().__init__(f"{what}: {status_string(code)} ({code}){detail}")
         self.code = code
 
 
@@ -89,6 +97,12 @@ def load_library(path: str | None = None):
         lib.fa_fwd_splitkv_gqa.restype = i
         lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_varlen.restype = i
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
+        lib.fa_bwd.restype = i
+        lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
+        lib.fa_bwd_workspace_bytes.restype = sz
+        lib.fa_last_error.argtypes = []
+        lib.fa_last_error.restype = ctypes.c_char_p
         lib.fa_splitkv_noalloc_capacity_bytes.argtypes = []
         lib.fa_splitkv_noalloc_capacity_bytes.restype = sz
         if path is None:
@@ -167,6 +181,63 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd" if H_kv == H else "fa_fwd_gqa")
     return out, lse
+
+
+def bwd_workspace_bytes(B, H, Nq, d) -> int:
+    return int(load_library().fa_bwd_workspace_bytes(B, H, Nq, d))
+
+
+def bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
+        workspace=None, stream=None):
+    """Attention backward through ``fa_bwd``: (dq, dk, dv) for the forward that gave
+    (o, lse) from (q, k, v) with the same causal flag and scale."""
+    B, H, H_kv, Nq, Nk, d = _check_qkv(q, k, v, allow_gqa=False)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    for name, t, shape in (("o", o, q.shape), ("dout", dout, q.shape)):
+        if not t.is_cuda or t.shape != shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous tensor like q")
+    if lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor")
+    outs = []
+    for name, t, like in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if t is None:
+            t = torch.empty_like(like)
+        elif t.shape != like.shape or t.dtype != like.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must match its input")
+        outs.append(t)
+    dq, dk, dv = outs
+    need = bwd_workspace_bytes(B, H, Nq, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    rc = load_library().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                               lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d,
+                               int(bool(causal)), scale, _dtype_code(q), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+class _Attention(torch.autograd.Function):
+    """Forward through fa_fwd, backward through fa_bwd."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, causal, scale):
+        o, lse = fwd(q, k, v, causal=causal, scale=scale)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.causal, ctx.scale = causal, scale
+        return o
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = bwd(q, k, v, o, dout.contiguous(), lse, causal=ctx.causal, scale=ctx.scale)
+        return dq, dk, dv, None, None
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None):
+    """Differentiable attention: fa_fwd in the forward pass, fa_bwd in the backward."""
+    return _Attention.apply(q, k, v, bool(causal), scale)
 
 
 def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal: bool = False,

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdio>
 #include <cstdint>
 #include <mutex>
 
@@ -38,16 +39,29 @@ DeviceState g_dev[kMaxDevices];
 void *g_scratch_addr[kMaxDevices];  // device address of g_splitkv_scratch, looked up once per device
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+// Why the calling thread last got FA_ERR_CUDA (read by fa_last_error).
+thread_local char t_last_error[160];
+
+int cuda_fail(const char *where, int code, const char *name) {
+    snprintf(t_last_error, sizeof(t_last_error), "%s failed: %s (%d)", where, name ? name : "CUresult", code);
+    return FA_ERR_CUDA;
+}
+int cuda_fail(const char *where, cudaError_t e) { return cuda_fail(where, (int)e, cudaGetErrorName(e)); }
+int launch_status(const char *what, cudaError_t e) { return e == cudaSuccess ? FA_OK : cuda_fail(what, e); }
+
 int dev_state(DeviceState **out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+    if (dev < 0 || dev >= kMaxDevices) return cuda_fail("device index", dev, "out of range");
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState &st = g_dev[dev];
     if (!st.ready) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return FA_ERR_CUDA;
+        if ((e = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
         int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FA_ERR_CUDA;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail("cudaDeviceGetAttribute", e);
         st.status = static_cast<int *>(p);
         st.num_sms = sms;
         st.ready = true;
@@ -58,7 +72,7 @@ int dev_state(DeviceState **out) {
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
                 cudaSuccess ||
             q != cudaDriverEntryPointSuccess || fn == nullptr)
-            return FA_ERR_CUDA;
+            return cuda_fail("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", (int)q, "no entry point");
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     *out = &st;
@@ -76,7 +90,7 @@ int make_map(CUtensorMap *map, const void *ptr, bool bf16, int d, int rows, int 
                           const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+    return r == CUDA_SUCCESS ? FA_OK : cuda_fail("cuTensorMapEncodeTiled", (int)r, nullptr);
 }
 
 // Packed [tokens][heads][d] 16-bit tensor of a variable-length batch: boxes of 64
@@ -91,7 +105,7 @@ int make_map_packed(CUtensorMap *map, const void *ptr, bool bf16, int d, int hea
                           const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+    return r == CUDA_SUCCESS ? FA_OK : cuda_fail("cuTensorMapEncodeTiled", (int)r, nullptr);
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -132,6 +146,8 @@ using namespace fa;
 extern "C" {
 
 int fa_version(void) { return 100; }
+
+const char *fa_last_error(void) { return t_last_error; }
 
 const char *fa_status_string(int status) {
     switch (status) {
@@ -189,7 +205,7 @@ int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
     a.causal = causal;
     a.scale_log2 = scale * 1.4426950408889634f;
     cudaError_t e = launch_fwd(d, bf16, tq, tk, tv, a, BH, reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return launch_status("kernel launch", e);
 }
 
 int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, const int *cu_seqlens_q,
@@ -226,7 +242,7 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *l
     a.causal = causal;
     a.scale_log2 = scale * 1.4426950408889634f;
     cudaError_t e = launch_fwd_varlen(d, bf16, tq, tk, tv, a, num_seqs, reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return launch_status("kernel launch", e);
 }
 
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq, int Nk, int d,
@@ -275,7 +291,7 @@ int fa_splitkv_combine(const float *o_part, const float *lse_part, void *o, floa
     a.num_splits = num_splits;
     a.rows = rows;
     cudaError_t e = launch_combine(d, dtype == FA_BF16, a, reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return launch_status("kernel launch", e);
 }
 
 int fa_fwd_splitkv_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int H_kv,
@@ -315,7 +331,7 @@ int fa_fwd_splitkv_gqa(const void *q, const void *k, const void *v, void *o, flo
     a.scale_log2 = scale * 1.4426950408889634f;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = launch_splitkv(d, bf16, tk, tv, a, s);
-    if (e != cudaSuccess) return FA_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_fail("kernel launch", e);
     return fa_splitkv_combine(o_part, lse_part, o, lse, num_splits, B, H, Nq, d, dtype, stream);
 }
 
@@ -326,19 +342,72 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *
                               workspace_bytes, stream);
 }
 
+size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || (d != 64 && d != 128)) return 0;
+    const size_t rows = (size_t)B * H * (size_t)((Nq + kBwdBr - 1) / kBwdBr) * kBwdBr;
+    return align256(rows * d * sizeof(float)) + 2 * align256(rows * sizeof(float));
+}
+
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse, void *dq,
+           void *dk, void *dv, int B, int H, int Nq, int Nk, int d, int causal, float scale, fa_dtype dtype,
+           void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+    int rc = check_common(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, dtype);
+    if (rc != FA_OK) return rc;
+    if (dout == nullptr || lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
+        return FA_ERR_INVALID_ARG;
+    if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16)) return FA_ERR_MISALIGNED;
+    if ((long long)B * H > 65535) return FA_ERR_INVALID_ARG;  // grid.y limit
+    const size_t need = fa_bwd_workspace_bytes(B, H, Nq, d);
+    if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    DeviceState *st = nullptr;
+    if ((rc = dev_state(&st)) != FA_OK) return rc;
+    const bool bf16 = dtype == FA_BF16;
+    const int BH = B * H;
+    const int Nq_pad = (Nq + kBwdBr - 1) / kBwdBr * kBwdBr;
+    CUtensorMap tq, tk, tv, tdo;
+    if (make_map(&tq, q, bf16, d, Nq, BH, kBwdBr) != FA_OK || make_map(&tk, k, bf16, d, Nk, BH, kBwdBc) != FA_OK ||
+        make_map(&tv, v, bf16, d, Nk, BH, kBwdBc) != FA_OK || make_map(&tdo, dout, bf16, d, Nq, BH, kBwdBr) != FA_OK)
+        return FA_ERR_CUDA;
+    const size_t rows = (size_t)BH * Nq_pad;
+    BwdArgs a;
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.dk = dk;
+    a.dv = dv;
+    a.dq = dq;
+    a.dq_acc = static_cast<float *>(workspace);
+    a.lse2 = reinterpret_cast<float *>(static_cast<char *>(workspace) + align256(rows * d * sizeof(float)));
+    a.dvec = reinterpret_cast<float *>(reinterpret_cast<char *>(a.lse2) + align256(rows * sizeof(float)));
+    a.status = st->status;
+    a.BH = BH;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.Nq_pad = Nq_pad;
+    a.causal = causal;
+    a.scale = scale;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    cudaError_t e = launch_bwd(d, bf16, tq, tk, tv, tdo, a, reinterpret_cast<cudaStream_t>(stream));
+    return launch_status("kernel launch", e);
+}
+
 int fa_get_device_status(fa_stream_t stream) {
     DeviceState *st = nullptr;
     int rc = dev_state(&st);
     if (rc != FA_OK) return rc;
-    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("cudaStreamSynchronize", e);
     int word = 0;
-    if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+    if ((e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof(int))) != cudaSuccess)
+        return cuda_fail("cudaMemcpyFromSymbol", e);
     if (word != 0) {
         const int zero = 0;
-        if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+        if ((e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int))) != cudaSuccess)
+            return cuda_fail("cudaMemcpyToSymbol", e);
         if (word & kDevErrTimeout) return FA_ERR_DEVICE_TIMEOUT;
+        if (word & kDevErrLayout) return cuda_fail("kernel", 0, "shared memory base not 1024-byte aligned");
     }
-    if (cudaPeekAtLastError() != cudaSuccess) return FA_ERR_CUDA;
+    if ((e = cudaPeekAtLastError()) != cudaSuccess) return cuda_fail("cudaPeekAtLastError", e);
     return FA_OK;
 }
 
@@ -360,13 +429,14 @@ int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o,
     // The scratch array's host-side name is not a device address: look the address
     // up once per device, with that device current, and pass it to the kernels.
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail("cudaGetDevice", cudaErrorInvalidDevice);
     void *scratch = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if (g_scratch_addr[dev] == nullptr) {
             void *p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_splitkv_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
+            if (cudaGetSymbolAddress(&p, g_splitkv_scratch) != cudaSuccess || p == nullptr)
+                return cuda_fail("cudaGetSymbolAddress", cudaErrorInvalidSymbol);
             g_scratch_addr[dev] = p;
         }
         scratch = g_scratch_addr[dev];
@@ -394,7 +464,7 @@ int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o,
     a.scale_log2 = scale * 1.4426950408889634f;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = launch_splitkv(d, bf16, tk, tv, a, s);
-    if (e != cudaSuccess) return FA_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_fail("kernel launch", e);
     return fa_splitkv_combine(o_part, lse_part, o, lse, num_splits, B, H, Nq, d, dtype, stream);
 }
 

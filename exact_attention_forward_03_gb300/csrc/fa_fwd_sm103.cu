@@ -534,8 +534,7 @@ static cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, co
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)num_m, (unsigned)rows_y, 1);
-    kern<<<grid, kFwdThreads, C::kSmemBytes, stream>>>(tq, tk, tv, a);
-    return cudaGetLastError();
+    return launch_kernel(kern, grid, dim3(kFwdThreads), C::kSmemBytes, stream, tq, tk, tv, a);
 }
 
 template <bool VARLEN>

@@ -10,6 +10,7 @@ namespace fa {
 
 // Device-side error bits OR-ed into the per-device status word.
 constexpr int kDevErrTimeout = 1;
+constexpr int kDevErrLayout = 2;  // a kernel found its shared memory base misaligned
 
 // Tile shape of the fused forward kernel: 128 query rows per Q tile (one TMEM
 // lane per row), one Q tile per CTA, 128 keys per K/V tile.
@@ -58,6 +59,26 @@ struct CombineArgs {
     long long rows;  // BH * Nq
 };
 
+// Backward: one CTA per 128-key block and head; query blocks of 128 rows.
+constexpr int kBwdBr = 128;
+constexpr int kBwdBc = 128;
+
+struct BwdArgs {
+    const void *o;      // [BH, Nq, d] 16-bit (forward output)
+    const void *dout;   // [BH, Nq, d] 16-bit
+    const float *lse;   // [BH, Nq] natural-log LSE of the forward
+    void *dk, *dv;      // [BH, Nk, d] 16-bit
+    void *dq;           // [BH, Nq, d] 16-bit
+    float *dq_acc;      // [BH, Nq_pad, d] fp32 workspace (zeroed by the preprocess kernel)
+    float *lse2;        // [BH, Nq_pad] LSE * log2(e); +inf for padding and rows that see no key
+    float *dvec;        // [BH, Nq_pad] D_i = rowsum(dO_i * O_i); 0 for padding
+    int *status;
+    int BH, Nq, Nk, Nq_pad;
+    int causal;
+    float scale;       // softmax scale
+    float scale_log2;  // scale * log2(e)
+};
+
 // Each launcher returns the CUDA error of the launch (cudaSuccess when queued).
 cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdArgs &a, int BH, cudaStream_t stream);
@@ -68,5 +89,8 @@ cudaError_t launch_fwd_varlen(int d, bool bf16, const CUtensorMap &tq, const CUt
 cudaError_t launch_splitkv(int d, bool bf16, const CUtensorMap &tk, const CUtensorMap &tv, const SplitArgs &a,
                            cudaStream_t stream);
 cudaError_t launch_combine(int d, bool bf16, const CombineArgs &a, cudaStream_t stream);
+// Backward: preprocess (D, lse2, zero dq_acc), the main K/V-block kernel, dQ conversion.
+cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream);
 
 }  // namespace fa

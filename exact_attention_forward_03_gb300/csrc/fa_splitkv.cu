@@ -278,8 +278,7 @@ static cudaError_t launch_splitkv_t(const CUtensorMap &tk, const CUtensorMap &tv
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const long long ctas = (long long)a.num_splits * a.Nq * a.BH;
-    kern<<<(unsigned)ctas, kSplitThreads, C::kSmemBytes, stream>>>(tk, tv, a);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3((unsigned)ctas), dim3(kSplitThreads), C::kSmemBytes, stream, tk, tv, a);
 }
 
 cudaError_t launch_splitkv(int d, bool bf16, const CUtensorMap &tk, const CUtensorMap &tv, const SplitArgs &a,
@@ -292,8 +291,7 @@ cudaError_t launch_splitkv(int d, bool bf16, const CUtensorMap &tk, const CUtens
 template <int D, bool BF16>
 static cudaError_t launch_combine_t(const CombineArgs &a, cudaStream_t stream) {
     const long long blocks = (a.rows + 3) / 4;
-    fa_combine_kernel<D, BF16><<<(unsigned)blocks, 128, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(fa_combine_kernel<D, BF16>, dim3((unsigned)blocks), dim3(128), 0, stream, a);
 }
 
 cudaError_t launch_combine(int d, bool bf16, const CombineArgs &a, cudaStream_t stream) {

@@ -233,6 +233,42 @@ FA_API int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, v
 FA_API size_t fa_splitkv_noalloc_capacity_bytes(void);
 
 /*
+ * Attention backward: the gradients dQ, dK, dV of O = softmax(scale * Q K^T +
+ * mask) V given dO, for the same mask as the forward ("Lecture 25" §3.3, the
+ * backward with P recomputed from the saved statistics; "02 · FA2:
+ * parallelism and work partitioning" §5, the K/V block outer loop with dQ
+ * accumulated across blocks):
+ *     P = exp(scale * Q K^T + mask - LSE),  dV = P^T dO,  dP = dO V^T,
+ *     dS = P o (dP - rowsum(dO o O)),  dQ = scale * dS K,  dK = scale * dS^T Q.
+ * Inputs: q, k, v, dtype and causal as given to the forward that produced o
+ * and lse (lse in natural-log units, as fa_fwd writes it; a row with LSE = -inf
+ * gets dQ = 0); dout is dO.  Layouts: q, o, dout, dq [B, H, Nq, d]; k, v, dk, dv
+ * [B, H, Nk, d]; lse [B, H, Nq] fp32; 16-bit tensors contiguous.  Outputs dq,
+ * dk, dv are fully overwritten (keys that no query sees get dK = dV = 0).
+ * Workspace: device memory of at least fa_bwd_workspace_bytes(B, H, Nq, d)
+ * bytes, 256-byte aligned, owned by the caller and free for reuse once the
+ * call's work on `stream` has finished; it holds an fp32 dQ accumulator and
+ * two per-row vectors.  The dQ sum over K/V blocks uses fp32 atomic adds, so
+ * dq may differ in the last bits between runs; dk and dv are deterministic.
+ * Three launches on `stream`: preprocess, the main kernel, dQ conversion.
+ * Errors: the common validation above; FA_ERR_INVALID_ARG for a null dout,
+ * lse, dq, dk or dv, or B * H > 65535; FA_ERR_MISALIGNED for dout, dq, dk, dv
+ * not 16-byte aligned; FA_ERR_WORKSPACE for a null, misaligned or short
+ * workspace.
+ */
+FA_API size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d);
+FA_API int fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse,
+                  void *dq, void *dk, void *dv, int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                  fa_dtype dtype, void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * The reason for the last FA_ERR_CUDA returned to the calling thread (the CUDA
+ * call that failed and its error name), or "" if there was none.  The string
+ * belongs to the library and stays valid until this thread's next call.
+ */
+FA_API const char *fa_last_error(void);
+
+/*
  * Synchronises `stream`, then returns FA_ERR_DEVICE_TIMEOUT if any kernel of
  * this library on the current device gave up a bounded wait since the last
  * call (the flag is cleared), FA_ERR_CUDA if the context reports an error,

@@ -66,3 +66,65 @@ def compare(o_gpu, o_ref: np.ndarray, lse_gpu, lse_ref: np.ndarray, dtype: torch
 
 def sdpa_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
+
+
+# ---------------------------------------------------------------- backward
+#
+# Tolerance of the gradients, from the arithmetic of the kernel.  With inputs
+# exactly representable in the 16-bit type and fp32 accumulation, the rounding
+# steps are: P to 16 bits (for dV), dS to 16 bits (for dK, dQ), D computed from
+# the 16-bit forward output O, and the final rounding of each gradient.  Each is
+# a relative error of at most u/2 (u = 2^-8 for bf16, 2^-11 for fp16) of the
+# rounded value, so with the magnitudes
+#     mag_dV = P^T |dO|,
+#     mag_dS = P o (|dP| + rowsum(|dO| o |O|)),
+#     mag_dK = scale mag_dS^T |Q|,   mag_dQ = scale mag_dS |K|,
+# every element satisfies |g_gpu - g_ref| <= u/2 (mag_g + |g_ref|) plus fp32
+# accumulation terms far below that.  The test allows twice that much,
+#     |g_gpu - g_ref| <= u (mag_g + |g_ref|) + floor,
+# where floor covers fp16 subnormals (P or dS below 2^-14 keep an absolute
+# error up to 2^-25): floor = 2^-25 x (number of summed terms) x max|operand|.
+
+GRAD_U = {torch.float16: 2.0 ** -11, torch.bfloat16: 2.0 ** -8}
+
+
+def grad_magnitudes(q, k, v, o, dout, lse, causal: bool, scale: float):
+    """(mag_dq, mag_dk, mag_dv) in fp64 for [BH, N, d] numpy arrays (lse [BH, Nq])."""
+    Nq, Nk = q.shape[-2], k.shape[-2]
+    allowed = np.ones((Nq, Nk), dtype=bool)
+    if causal:
+        allowed = np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq)
+    mags = [np.empty(q.shape), np.empty(k.shape), np.empty(v.shape)]
+    for b in range(q.shape[0]):
+        s = scale * (q[b] @ k[b].T)
+        with np.errstate(invalid="ignore", over="ignore"):
+            p = np.exp(s - lse[b][:, None])
+        p = np.where(allowed & np.isfinite(lse[b])[:, None], p, 0.0)
+        del s
+        dp = np.abs(dout[b] @ v[b].T)
+        mag_d = (np.abs(dout[b]) * np.abs(o[b])).sum(axis=1)
+        mag_ds = p * (dp + mag_d[:, None])
+        del dp
+        mags[0][b] = scale * (mag_ds @ np.abs(k[b]))
+        mags[1][b] = scale * (mag_ds.T @ np.abs(q[b]))
+        mags[2][b] = p.T @ np.abs(dout[b])
+    return tuple(mags)
+
+
+def compare_grads(got, ref, mags, floors, dtype: torch.dtype, what: str = ""):
+    """Assert |g_gpu - g_ref| <= u (mag + |g_ref|) + floor for g in (dq, dk, dv)."""
+    u = GRAD_U[dtype]
+    stats = {}
+    for name, g, r, m, fl in zip(("dq", "dk", "dv"), got, ref, mags, floors):
+        gg = g.detach().to("cpu").to(torch.float64).numpy().reshape(r.shape)
+        assert np.isfinite(gg).all(), f"{what}: non-finite {name}"
+        err = np.abs(gg - r)
+        tol = u * (m + np.abs(r)) + fl
+        stats[name + "_max_err"] = float(err.max(initial=0.0))
+        stats[name + "_max_err_over_tol"] = float((err / tol).max(initial=0.0))
+        bad = err > tol
+        if bad.any():
+            idx = np.unravel_index(np.argmax(err / tol), err.shape)
+            raise AssertionError(f"{what}: {int(bad.sum())} {name} elements out of tolerance; worst at {idx}: "
+                                 f"gpu={gg[idx]!r} ref={r[idx]!r} tol={tol[idx]!r}")
+    return stats
