@@ -54,6 +54,14 @@ int dev_state(DeviceState **out) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
     if (dev < 0 || dev >= kMaxDevices) return cuda_fail("device index", dev, "out of range");
+    // The tensor-map encoder is a driver call and needs a current context; a thread
+    // that has made no runtime call yet (an autograd worker, say) has none.  Setting
+    // the device once per thread makes its primary context current.
+    thread_local int t_ctx_dev = -1;
+    if (t_ctx_dev != dev) {
+        if ((e = cudaSetDevice(dev)) != cudaSuccess) return cuda_fail("cudaSetDevice", e);
+        t_ctx_dev = dev;
+    }
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState &st = g_dev[dev];
     if (!st.ready) {

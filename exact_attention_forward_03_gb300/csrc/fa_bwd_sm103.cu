@@ -29,21 +29,22 @@
 // blocks of 128-byte swizzled rows, which the tensor core reads K-major in the
 // first two products and MN-major in the last ones: no tile is stored twice.
 //
-// Roles (10 warps):
-//   warps 0-7  warp w works on key lanes 32 (w % 4) ... + 31 and query columns
-//              64 (w / 4) ... + 63: P, then dS, then the dQ read-out of the same
-//              columns (for d = 128, lanes of dQ^T are head-dim indices), then
-//              the dK, dV epilogue
-//   warp 8     TMA: K_j and V_j once; Q_i with its LSE and D vectors, and dO_i,
-//              through two-slot rings
-//   warp 9     owns tensor memory; one lane issues every MMA
+// Roles (16 warps, four warpgroups):
+//   warps 0-7   elementwise: warp w works on key lanes 32 (w % 4) ... + 31 and query
+//               columns 64 (w / 4) ... + 63 (P, then dS), then the dK, dV epilogue
+//   warps 8-11  dQ writers: read dQ(t) out of tensor memory (for d = 128 the lanes
+//               of dQ^T are head-dim indices, so a warp's atomic adds cover 32
+//               consecutive floats of a dQ row) and add it to the fp32 accumulator
+//   warp 12     TMA: K_j and V_j once; Q_t with its LSE and D vectors, and dO_t,
+//               through two-slot rings
+//   warp 13     owns tensor memory; one lane issues every MMA
 //
-// Order on the tensor core per block i: S(i), dP(i), dV(i), dK(i), dQ(i).  S(i)
-// overwrites P(i-1) only after dV(i-1) completed; for d = 128, dP(i) overwrites
-// dQ(i-1) only after the elementwise warps read it out, which they do while S(i)
-// runs.  P(i) is computed while dP(i) runs and dS(i) while dV(i) runs, so the
-// tensor core waits only when the exponentials take longer than one product.
-// Every barrier is used once per block, so parities are (i & 1); no waiter can
+// Order on the tensor core per block t: dP(t), dV(t), S(t+1), dK(t), dQ(t).  S(t+1)
+// overwrites P(t) once dV(t) completed and runs ahead of dK(t) and dQ(t), so the
+// elementwise warps compute P(t+1) while the tensor core finishes block t; P(t)
+// overlaps dP(t) and dS(t) overlaps dV(t).  For d = 128, dQ^T(t) lives in the
+// columns of dP and dP(t+1) waits until the writers have read it out.
+// Every barrier is used once per block, so parities are (t & 1); no waiter can
 // fall two phases behind because each producer waits on the consumer of its
 // previous phase before it produces again.
 //
@@ -51,14 +52,23 @@
 // status word, stops issuing, waits (bounded) for its loads and MMAs in flight,
 // frees tensor memory and exits.
 #include <algorithm>
+#include <climits>
 
 #include "fa_device.cuh"
 #include "fa_internal.h"
 
 namespace fa {
 
-constexpr int kBwdThreads = 320;
-constexpr int kBwdWarpTma = 8, kBwdWarpMma = 9;
+constexpr int kBwdEwWarps = 8;                    // warps 0-7: elementwise (warpgroups 0, 1)
+constexpr int kBwdWarpDq0 = 8;                    // warps 8-11: dQ writers (warpgroup 2)
+constexpr int kBwdWarpTma = 12, kBwdWarpMma = 13; // warpgroup 3 (warps 14, 15 idle)
+constexpr int kBwdThreads = 16 * 32;
+// Registers: the launch gives every thread 128 (65536 / 512).  Warpgroup 3 drops to
+// 72 and the other three rise to 144; each SM sub-partition holds one warp of every
+// warpgroup, and 3 x 144 + 72 = 504 <= 4 x 128 per thread slot.
+constexpr uint32_t kBwdRegsLaunch = 128, kBwdRegsWork = 144, kBwdRegsIo = 72;
+static_assert(3 * kBwdRegsWork + kBwdRegsIo <= 4 * kBwdRegsLaunch, "register split exceeds the launch");
+static_assert(kBwdRegsLaunch * kBwdThreads <= 65536, "launch registers");
 
 template <int D>
 struct BwdCfg {
@@ -90,6 +100,31 @@ struct BwdCfg {
     static constexpr uint32_t kTmemDQ = (D == 128) ? 128u : 256u + 2u * D;
     static constexpr uint32_t kTmemCols = 512;
 };
+
+// P for one thread's key and 32 query columns: p = 2^(s scale log2(e) + nl2) with
+// nl2 = -LSE log2(e) of each query row (-inf on rows that see no key).  MASKED adds
+// the causal mask (query q sees key j when q >= qmin) and the ragged end of the keys.
+template <bool MASKED>
+__device__ __forceinline__ void bwd_p_chunk(const uint32_t (&sv)[32], const float *nl2, float sl2, int q_first,
+                                            int qmin, bool key_ok, float *p) {
+    const uint64_t sl2x2 = f2_make(sl2, sl2);
+#pragma unroll
+    for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 L = reinterpret_cast<const float4 *>(nl2)[e4];
+        const float2 x01 = f2_split(ffma2(f2_make(__uint_as_float(sv[4 * e4]), __uint_as_float(sv[4 * e4 + 1])),
+                                          sl2x2, f2_make(L.x, L.y)));
+        const float2 x23 = f2_split(ffma2(f2_make(__uint_as_float(sv[4 * e4 + 2]), __uint_as_float(sv[4 * e4 + 3])),
+                                          sl2x2, f2_make(L.z, L.w)));
+        float v[4] = {ex2_approx(x01.x), ex2_approx(x01.y), ex2_approx(x23.x), ex2_approx(x23.y)};
+        if constexpr (MASKED) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (!key_ok || q_first + 4 * e4 + u < qmin) v[u] = 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) p[4 * e4 + u] = v[u];
+    }
+}
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -132,11 +167,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto B_DOEMPTY = [](int s) { return 1 + 3 * S_ + s; };
     constexpr int B_SFULL = 1 + 4 * S_;
     constexpr int B_DPFULL = B_SFULL + 1;
-    constexpr int B_PREADY = B_SFULL + 2;   // 8 arrivals: one per elementwise warp
-    constexpr int B_DSREADY = B_SFULL + 3;  // 8 arrivals
+    constexpr int B_PREADY = B_SFULL + 2;   // one arrival per elementwise warp
+    constexpr int B_DSREADY = B_SFULL + 3;  // one arrival per elementwise warp
     constexpr int B_DVDONE = B_SFULL + 4;
     constexpr int B_DQFULL = B_SFULL + 5;
-    constexpr int B_DQFREE = B_SFULL + 6;   // 8 arrivals
+    constexpr int B_DQFREE = B_SFULL + 6;   // one arrival per dQ-writer warp
     constexpr int B_DSFREE = B_SFULL + 7;
     constexpr int B_FINAL = B_SFULL + 8;
     constexpr int B_MMAFIN = B_SFULL + 9;
@@ -154,11 +189,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mbar_init(bar(B_SFULL), 1);
         mbar_init(bar(B_DPFULL), 1);
-        mbar_init(bar(B_PREADY), 8);
-        mbar_init(bar(B_DSREADY), 8);
+        mbar_init(bar(B_PREADY), kBwdEwWarps);
+        mbar_init(bar(B_DSREADY), kBwdEwWarps);
         mbar_init(bar(B_DVDONE), 1);
         mbar_init(bar(B_DQFULL), 1);
-        mbar_init(bar(B_DQFREE), 8);
+        mbar_init(bar(B_DQFREE), 4);
         mbar_init(bar(B_DSFREE), 1);
         mbar_init(bar(B_FINAL), 1);
         mbar_init(bar(B_MMAFIN), 1);
@@ -180,7 +215,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tmem = *tmem_holder;
     constexpr uint32_t hi = sdesc_hi_sw128(1024);  // 8 rows x 128 B per core group
 
-    if (warp == kBwdWarpTma) {
+    if (warp >= kBwdWarpTma) {
+      // Warpgroup 3: TMA producer and MMA issuer, one lane each.
+      regs_decrease<kBwdRegsIo>();
+      if (warp == kBwdWarpTma) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && n > 0) {
             uint32_t pend_q = 0, pend_do = 0, par_q = 0, par_do = 0;
@@ -195,7 +233,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int s = t % S_;
                 const uint32_t it = (uint32_t)(t / S_);
                 const int q0 = (i_start + t) * kBwdBr;
-                ok = mbar_wait_backoff(bar(B_QEMPTY(s)), (it & 1u) ^ 1u, abort_flag, status, 64);
+                ok = mbar_wait_backoff(bar(B_QEMPTY(s)), (it & 1u) ^ 1u, abort_flag, status, 32);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(B_QFULL(s)), C::kTileBytes + C::kVecBytes);
                 for (int b = 0; b < C::kBlocks; ++b)
@@ -206,7 +244,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 bulk_load(vdst + 512, args.dvec + vec_row + q0, 512, bar(B_QFULL(s)));
                 pend_q |= 1u << s;
                 par_q = (par_q & ~(1u << s)) | ((it & 1u) << s);
-                ok = mbar_wait_backoff(bar(B_DOEMPTY(s)), (it & 1u) ^ 1u, abort_flag, status, 64);
+                ok = mbar_wait_backoff(bar(B_DOEMPTY(s)), (it & 1u) ^ 1u, abort_flag, status, 32);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(B_DOFULL(s)), C::kTileBytes);
                 for (int b = 0; b < C::kBlocks; ++b)
@@ -223,7 +261,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (pend_do & (1u << s)) mbar_wait_bounded(bar(B_DOFULL(s)), (par_do >> s) & 1u, &no_abort, status);
             }
         }
-    } else if (warp == kBwdWarpMma) {
+      } else if (warp == kBwdWarpMma) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n > 0) {
             constexpr uint32_t idesc_s = idesc_f16(128, 128, BF16, false, false);  // S^T, dP^T
@@ -235,26 +273,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint32_t k_mn = sdesc_lo(sb + C::kOffK, C::kBlockBytes);      // MN-major: LBO = block
             const uint32_t ds_k = sdesc_lo(sb + C::kOffDS, 16);
             const uint32_t ds_mn = sdesc_lo(sb + C::kOffDS, C::kBlockBytes);
-            bool ok = mbar_wait_bounded(bar(B_KV), 0, abort_flag, status);
-            for (int t = 0; ok && t < n; ++t) {
-                const int s = t % S_;
-                const uint32_t ph = (uint32_t)(t / S_) & 1u;
-                const uint32_t pt = (uint32_t)t & 1u, pp = (uint32_t)(t - 1) & 1u;
-                // S^T(i) = K Q_i^T into [0,128), once dV(i-1) has read P(i-1) from there.
-                ok = mbar_wait_backoff(bar(B_QFULL(s)), ph, abort_flag, status, 32) &&
-                     (t == 0 || mbar_wait_backoff(bar(B_DVDONE), pp, abort_flag, status, 32));
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t q_lo = sdesc_lo(sb + C::kOffQ + s * C::kTileBytes, 16);
+            // S^T(t) = K Q_t^T into [0,128).
+            auto issue_s = [&](int t) {
+                const uint32_t q_lo = sdesc_lo(sb + C::kOffQ + (t % S_) * C::kTileBytes, 16);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (uint32_t)((k >> 2) * C::kBlockBytes + (k & 3) * 32) >> 4;
                     umma_ss_w(tmem + C::kTmemS, k_lo + off, hi, q_lo + off, hi, idesc_s, k > 0 ? 1u : 0u);
                 }
                 umma_commit(bar(B_SFULL));
-                // dP^T(i) = V dO_i^T into [128,256); for d = 128 once dQ^T(i-1) has been read out.
+            };
+            bool ok = mbar_wait_bounded(bar(B_KV), 0, abort_flag, status) &&
+                      mbar_wait_backoff(bar(B_QFULL(0)), 0, abort_flag, status, 32);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+            }
+            for (int t = 0; ok && t < n; ++t) {
+                const int s = t % S_;
+                const uint32_t ph = (uint32_t)(t / S_) & 1u;
+                const uint32_t pt = (uint32_t)t & 1u, pp = (uint32_t)(t - 1) & 1u;
+                // dP^T(t) = V dO_t^T into [128,256); for d = 128 once dQ^T(t-1) has been read out.
                 ok = mbar_wait_backoff(bar(B_DOFULL(s)), ph, abort_flag, status, 32) &&
-                     (D != 128 || t == 0 || mbar_wait_backoff(bar(B_DQFREE), pp, abort_flag, status, 32));
+                     (D != 128 || t == 0 || mbar_wait_bounded(bar(B_DQFREE), pp, abort_flag, status));
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t do_lo = sdesc_lo(sb + C::kOffDO + s * C::kTileBytes, 16);
@@ -264,8 +305,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     umma_ss_w(tmem + C::kTmemDP, v_lo + off, hi, do_lo + off, hi, idesc_s, k > 0 ? 1u : 0u);
                 }
                 umma_commit(bar(B_DPFULL));
-                // dV += P^T dO_i: P^T from tensor memory, 16 queries per instruction.
-                ok = mbar_wait_backoff(bar(B_PREADY), pt, abort_flag, status, 32);
+                // dV += P^T dO_t: P^T from tensor memory, 16 queries per instruction.
+                ok = mbar_wait_bounded(bar(B_PREADY), pt, abort_flag, status);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t do_mn = sdesc_lo(sb + C::kOffDO + s * C::kTileBytes, C::kBlockBytes);
@@ -275,8 +316,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                               do_mn + (uint32_t)((k * 2048) >> 4), hi, idesc_kv, (t > 0 || k > 0) ? 1u : 0u);
                 umma_commit(bar(B_DVDONE));
                 umma_commit(bar(B_DOEMPTY(s)));
-                // dK += dS^T Q_i.
-                ok = mbar_wait_backoff(bar(B_DSREADY), pt, abort_flag, status, 32);
+                // S^T(t+1) next, so that the elementwise warps can start on P(t+1) while the
+                // tensor core does dK(t) and dQ(t); it overwrites P(t) once dV(t) completed.
+                if (t + 1 < n) {
+                    ok = mbar_wait_backoff(bar(B_QFULL((t + 1) % S_)), (uint32_t)((t + 1) / S_) & 1u, abort_flag,
+                                           status, 32) &&
+                         mbar_wait_bounded(bar(B_DVDONE), pt, abort_flag, status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(t + 1);
+                }
+                // dK += dS^T Q_t.
+                ok = mbar_wait_bounded(bar(B_DSREADY), pt, abort_flag, status);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t q_mn = sdesc_lo(sb + C::kOffQ + s * C::kTileBytes, C::kBlockBytes);
@@ -287,9 +338,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                               (t > 0 || k > 0) ? 1u : 0u);
                 }
                 umma_commit(bar(B_QEMPTY(s)));
-                // dQ(i): for d = 64 into its own columns, once dQ(i-1) has been read out.
+                // dQ(t): for d = 64 into its own columns, once dQ(t-1) has been read out.
                 if (D != 128 && t > 0) {
-                    ok = mbar_wait_backoff(bar(B_DQFREE), pp, abort_flag, status, 32);
+                    ok = mbar_wait_bounded(bar(B_DQFREE), pp, abort_flag, status);
                     if (!ok) break;
                     tc_fence_after();
                 }
@@ -310,14 +361,67 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             volatile int no_abort = 0;
             mbar_wait_bounded(bar(B_MMAFIN), 0, &no_abort, status);
         }
+      }
+    } else if (warp >= kBwdWarpDq0) {
+        // ------------------------------------------------------------ dQ writers
+        // All of dQ(t) is read from tensor memory at once (its columns are released for
+        // dP(t+1) right away), then summed into the fp32 accumulator.
+        regs_increase<kBwdRegsWork>();
+        const int qw = warp & 3;
+        const uint32_t lane_base = tmem + ((uint32_t)(qw * 32) << 16);
+        bool ok = true;
+        for (int t = 0; t < n; ++t) {
+            const int q0 = (i_start + t) * kBwdBr;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_DQFULL), (uint32_t)t & 1u, abort_flag, status));
+            if (!ok) break;
+            tc_fence_after();
+            if constexpr (D == 128) {
+                // dQ^T: lane = head-dim index, columns = the block's 128 queries; a warp's
+                // 32 lanes add to 32 consecutive floats of one dQ row.
+                uint32_t a[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t (&ac)[32] = *reinterpret_cast<uint32_t(*)[32]>(a + 32 * c);
+                    tmem_ld_32x32b_x32(lane_base + C::kTmemDQ + 32 * c, ac);
+                }
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_DQFREE));
+                float *dst = args.dq_acc + ((size_t)bh * Nq_pad + q0) * 128 + qw * 32 + lane;
+                const int rows = Nq - q0;
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c < rows) atomicAdd(dst + (size_t)c * 128, __uint_as_float(a[c]));
+            } else {
+                // dQ: lane = query row q0 + 32 qw + lane, columns = the 64 head-dim indices.
+                uint32_t a[64];
+                tmem_ld_32x32b_x32(lane_base + C::kTmemDQ, *reinterpret_cast<uint32_t(*)[32]>(a));
+                tmem_ld_32x32b_x32(lane_base + C::kTmemDQ + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_DQFREE));
+                const int q = q0 + qw * 32 + lane;
+                if (q < Nq) {
+                    float4 *dst = reinterpret_cast<float4 *>(args.dq_acc + ((size_t)bh * Nq_pad + q) * 64);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        atomicAdd(dst + e, make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
+                                                       __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3])));
+                }
+            }
+        }
     } else {
-        // ------------------------------------------------------------ elementwise, dQ read-out, epilogue
+        // ------------------------------------------------------------ elementwise and epilogue
+        regs_increase<kBwdRegsWork>();
         const int qw = warp & 3;  // TMEM lanes [32 qw, 32 qw + 32)
         const int g = warp >> 2;  // query columns [64 g, 64 g + 64) of each block
         const int r = qw * 32 + lane;
         const int j = k0 + r;     // this thread's key
         const bool key_ok = j < Nk;
-        const int qmin = j - (Nk - Nq);  // causal: the first query row that sees key j
+        const int qmin = causal ? j - (Nk - Nq) : INT_MIN;  // the first query row that sees key j
+        const bool tail_block = k0 + kBwdBc > Nk;
         const uint32_t lane_base = tmem + ((uint32_t)(qw * 32) << 16);
         const float sl2 = args.scale_log2;
         float p[64];
@@ -326,33 +430,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int s = t % S_;
             const uint32_t pt = (uint32_t)t & 1u;
             const int q0 = (i_start + t) * kBwdBr;
-            const bool masked = causal && (q0 + (Nk - Nq) < k0 + kBwdBc - 1);
+            const bool masked = tail_block || (causal && (q0 + (Nk - Nq) < k0 + kBwdBc - 1));
             // ---- P = 2^(S scale log2(e) - LSE log2(e)) for this thread's key and 64 queries
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_QFULL(s)), (uint32_t)(t / S_) & 1u, abort_flag,
                                                            status) &&
                                              mbar_wait_bounded(bar(B_SFULL), pt, abort_flag, status));
             if (!ok) break;
             tc_fence_after();
-            const float *lse2 = reinterpret_cast<const float *>(smem + C::kOffVec + s * C::kVecBytes);
-            const float *dvec = lse2 + 128;
+            const float *nl2 = reinterpret_cast<const float *>(smem + C::kOffVec + s * C::kVecBytes);
+            const float *ndv = nl2 + 128;
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t sv[32];
                 tmem_ld_32x32b_x32(lane_base + C::kTmemS + 64 * g + 32 * cc, sv);
                 tmem_wait_ld();
-                const float4 *l4 = reinterpret_cast<const float4 *>(lse2 + 64 * g + 32 * cc);
-#pragma unroll
-                for (int e4 = 0; e4 < 8; ++e4) {
-                    const float4 L = l4[e4];
-                    const float lv[4] = {L.x, L.y, L.z, L.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int c = 32 * cc + 4 * e4 + u;
-                        float pe = ex2_approx(fmaf(__uint_as_float(sv[4 * e4 + u]), sl2, -lv[u]));
-                        if (masked && q0 + 64 * g + c < qmin) pe = 0.f;
-                        p[c] = key_ok ? pe : 0.f;
-                    }
-                }
+                const int col = 64 * g + 32 * cc;
+                if (masked)
+                    bwd_p_chunk<true>(sv, nl2 + col, sl2, q0 + col, qmin, key_ok, p + 32 * cc);
+                else
+                    bwd_p_chunk<false>(sv, nl2 + col, sl2, q0 + col, qmin, key_ok, p + 32 * cc);
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) pk[e] = PK::pack(p[32 * cc + 2 * e], p[32 * cc + 2 * e + 1]);
@@ -374,18 +470,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 uint32_t dp[32];
                 tmem_ld_32x32b_x32(lane_base + C::kTmemDP + 64 * g + 32 * cc, dp);
                 tmem_wait_ld();
-                const float4 *d4 = reinterpret_cast<const float4 *>(dvec + 64 * g + 32 * cc);
+                const float4 *d4 = reinterpret_cast<const float4 *>(ndv + 64 * g + 32 * cc);
                 uint32_t pk[16];
 #pragma unroll
                 for (int e4 = 0; e4 < 8; ++e4) {
                     const float4 Dv = d4[e4];
                     const int c = 32 * cc + 4 * e4;
-                    const float d0 = p[c] * (__uint_as_float(dp[4 * e4]) - Dv.x);
-                    const float d1 = p[c + 1] * (__uint_as_float(dp[4 * e4 + 1]) - Dv.y);
-                    const float d2 = p[c + 2] * (__uint_as_float(dp[4 * e4 + 2]) - Dv.z);
-                    const float d3 = p[c + 3] * (__uint_as_float(dp[4 * e4 + 3]) - Dv.w);
-                    pk[2 * e4] = PK::pack(d0, d1);
-                    pk[2 * e4 + 1] = PK::pack(d2, d3);
+                    const float2 d01 = f2_split(fmul2(f2_make(p[c], p[c + 1]),
+                                                      fadd2(f2_make(__uint_as_float(dp[4 * e4]), __uint_as_float(dp[4 * e4 + 1])),
+                                                            f2_make(Dv.x, Dv.y))));
+                    const float2 d23 = f2_split(fmul2(f2_make(p[c + 2], p[c + 3]),
+                                                      fadd2(f2_make(__uint_as_float(dp[4 * e4 + 2]), __uint_as_float(dp[4 * e4 + 3])),
+                                                            f2_make(Dv.z, Dv.w))));
+                    pk[2 * e4] = PK::pack(d01.x, d01.y);
+                    pk[2 * e4 + 1] = PK::pack(d23.x, d23.y);
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -398,44 +496,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_DSREADY));
-            // ---- dQ read-out, summed into the fp32 accumulator
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_DQFULL), pt, abort_flag, status));
-            if (!ok) break;
-            tc_fence_after();
-            if constexpr (D == 128) {
-                // dQ^T: lane = head-dim index r, columns = this warp's 64 queries; a warp's
-                // 32 lanes add to 32 consecutive floats of one dQ row.
-                uint32_t a0[32], a1[32];
-                tmem_ld_32x32b_x32(lane_base + C::kTmemDQ + 64 * g, a0);
-                tmem_ld_32x32b_x32(lane_base + C::kTmemDQ + 64 * g + 32, a1);
-                tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_DQFREE));
-                float *dst = args.dq_acc + ((size_t)bh * Nq_pad + q0 + 64 * g) * 128 + r;
-                const int rows = min(64, Nq - (q0 + 64 * g));
-#pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    if (c < rows) atomicAdd(dst + (size_t)c * 128, __uint_as_float(a0[c]));
-#pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    if (c + 32 < rows) atomicAdd(dst + (size_t)(c + 32) * 128, __uint_as_float(a1[c]));
-            } else {
-                // dQ: lane = query row q0 + r, columns = head-dim indices 32 g ... + 31.
-                uint32_t a0[32];
-                tmem_ld_32x32b_x32(lane_base + C::kTmemDQ + 32 * g, a0);
-                tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_DQFREE));
-                if (q0 + r < Nq) {
-                    float4 *dst = reinterpret_cast<float4 *>(args.dq_acc + ((size_t)bh * Nq_pad + q0 + r) * 64 + 32 * g);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        atomicAdd(dst + e, make_float4(__uint_as_float(a0[4 * e]), __uint_as_float(a0[4 * e + 1]),
-                                                       __uint_as_float(a0[4 * e + 2]), __uint_as_float(a0[4 * e + 3])));
-                }
-            }
         }
         if (ok && n > 0) {
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_FINAL), 0, abort_flag, status));
@@ -486,8 +546,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 }
 
-// D_i = dO_i . O_i (fp32), lse2_i = LSE_i log2(e) (+inf where LSE_i = -inf and on
-// the padding rows Nq <= i < Nq_pad, so that P = 2^(x - lse2) = 0 there), and the
+// -D_i = -dO_i . O_i (fp32), -lse2_i = -LSE_i log2(e) (-inf where LSE_i = -inf and
+// on the padding rows Nq <= i < Nq_pad, so that P = 2^(x - lse2) = 0 there), and the
 // row of the dQ accumulator zeroed.  One warp per row of [BH][Nq_pad].
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdArgs a) {
@@ -515,9 +575,9 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdArgs a) {
             const float lse = a.lse[(size_t)bh * a.Nq + q];
             l2 = (lse == -INFINITY) ? INFINITY : lse * 1.4426950408889634f;
         }
-        if (lane == 0) {
-            a.dvec[row] = dot;
-            a.lse2[row] = l2;
+        if (lane == 0) {  // stored negated: the main kernel adds them
+            a.dvec[row] = -dot;
+            a.lse2[row] = -l2;
         }
     }
 }

@@ -70,8 +70,8 @@ struct BwdArgs {
     void *dk, *dv;      // [BH, Nk, d] 16-bit
     void *dq;           // [BH, Nq, d] 16-bit
     float *dq_acc;      // [BH, Nq_pad, d] fp32 workspace (zeroed by the preprocess kernel)
-    float *lse2;        // [BH, Nq_pad] LSE * log2(e); +inf for padding and rows that see no key
-    float *dvec;        // [BH, Nq_pad] D_i = rowsum(dO_i * O_i); 0 for padding
+    float *lse2;        // [BH, Nq_pad] -LSE * log2(e); -inf for padding and rows that see no key
+    float *dvec;        // [BH, Nq_pad] -D_i = -rowsum(dO_i * O_i); 0 for padding
     int *status;
     int BH, Nq, Nk, Nq_pad;
     int causal;
