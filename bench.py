@@ -9,7 +9,8 @@ stream, with the L2 cache flushed (a 256 MiB write) before each timed launch.
 The split-KV decode path (B=32, H=32, Nq=1, Nk=16384, d=128, bf16, 16 splits)
 is timed the same way and reported under "decode" in GB/s, and its grouped-query
 form (32 query heads over 8 K/V heads) under "decode_gqa".  The backward of the
-default workload (fa_bwd, 2.5x the forward's FLOPs) is reported under "bwd".
+default workload (fa_bwd, 2.5x the forward's FLOPs) is reported under "bwd", and
+its FP8 (E4M3) forward from pre-quantized inputs under "fp8".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fa|reference]
 
@@ -415,6 +416,38 @@ def run_fa(args, rank, world, local):
         del gout, gq, gk, gv, gws
         torch.cuda.empty_cache()
 
+    # ---- FP8 (E4M3) forward of the same workload from pre-quantized inputs
+    fp8 = None
+    if not args.no_fp8 and w.d == 128:
+        q8, qs = fa.fp8_quantize(q)
+        k8, ks = fa.fp8_quantize(k)
+        v8t, vs = fa.fp8_quantize(v, transpose=True)
+        o8 = torch.empty_like(o)
+
+        def qcall():
+            fa.fp8_quantize(q, out=q8, scales=qs)
+            fa.fp8_quantize(k, out=k8, scales=ks)
+            fa.fp8_quantize(v, transpose=True, out=v8t, scales=vs)
+
+        def fcall():
+            fa.fwd_fp8(q8, qs, k8, ks, v8t, vs, causal=w.causal, scale=w.scale, out_dtype=q.dtype, out=o8, lse=lse)
+
+        fms = time_calls(fcall, args.steps, args.warmup, flush)
+        qms = time_calls(qcall, max(3, min(args.steps, 20)), args.warmup, flush)
+        launches += args.steps + 3 * max(3, min(args.steps, 20))
+        fmean = statistics.mean(fms)
+        fpeak = 2.0 * peaks["bf16_tflops"]  # E4M3 dense rate = 2x bf16 (nominal 4.5 vs 2.25 PFLOP/s)
+        fach = flops / (fmean * 1e-3) / 1e12
+        fp8 = {"workload": w.name, "entry_point": "fa_fwd_fp8", "ms_per_call": fmean, "ms_min": min(fms),
+               "value": sum_over_ranks(flops, world) / (max_over_ranks(fmean, world) * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "quantize_ms_per_call": statistics.mean(qms),
+               "roofline": {"bound": "tensor", "achieved": fach, "peak": fpeak, "unit": "TFLOP/s", "frac": fach / fpeak,
+                            "traffic": None,
+                            "note": "inputs quantized beforehand (fa_fp8_quantize of Q, K, V timed separately as "
+                                    "quantize_ms_per_call); peak = 2 x measured bf16 (the E4M3/bf16 nominal ratio)"}}
+        del q8, k8, v8t, o8
+        torch.cuda.empty_cache()
+
     decode = decode_gqa = None
     if not args.no_decode:
         del q, k, v
@@ -474,7 +507,7 @@ def run_fa(args, rank, world, local):
                      "peak_source": peak_src,
                      "kernel": "fa_fwd_kernel<128,bf16>", "flops_per_launch": flops},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "decode": decode,
-        "decode_gqa": decode_gqa, "varlen": varlen, "bwd": bwd,
+        "decode_gqa": decode_gqa, "varlen": varlen, "bwd": bwd, "fp8": fp8,
         "wall_s_fwd_timed": wall, "ms_fwd_min": min(ms), "ms_fwd_median": statistics.median(ms),
     }
     if rank == 0:
@@ -515,6 +548,7 @@ def main(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-varlen", action="store_true")
     ap.add_argument("--no-bwd", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

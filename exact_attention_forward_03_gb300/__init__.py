@@ -12,6 +12,8 @@ Functions (same names as the C ABI without the ``fa_`` prefix):
     splitkv_combine(o_part, lse_part, out=None, lse=None, dtype=...)      -> (o, lse)
     bwd(q, k, v, o, dout, lse, causal=False, scale=None, ...)            -> (dq, dk, dv)
     attention(q, k, v, causal=False, scale=None)   differentiable: fwd, then bwd in backward
+    fp8_quantize(x, transpose=False) -> (codes, scales);  fwd_fp8(q8, qs, k8, ks, v8t, vs, ...) -> (o, lse)
+    fwd_fp8_from(q, k, v, causal=False) -> (o, lse)       quantize, then the FP8 forward
     splitkv_num_splits, splitkv_split_len, splitkv_workspace_bytes, bwd_workspace_bytes,
     get_device_status, status_string, version
 Tensors are ``[B, H, N, d]`` contiguous fp16 or bf16 on one CUDA device;
@@ -42,7 +44,7 @@ FA_ERR_SCRATCH_LIMIT = -7
 EXPORTS = ("fa_fwd", "fa_fwd_splitkv", "fa_splitkv_combine", "fa_splitkv_workspace_bytes",
            "fa_splitkv_num_splits", "fa_splitkv_split_len", "fa_get_device_status", "fa_status_string",
            "fa_version", "fa_fwd_splitkv_noalloc", "fa_splitkv_noalloc_capacity_bytes", "fa_fwd_gqa",
-           "fa_fwd_splitkv_gqa", "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace_bytes", "fa_last_error")
+           "fa_fwd_splitkv_gqa", "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace_bytes", "fa_last_error", "fa_fp8_quantize", "fa_fwd_fp8")
 
 _lock = threading.Lock()
 _lib = None
@@ -101,6 +103,10 @@ def load_library(path: str | None = None):
         lib.fa_bwd.restype = i
         lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
         lib.fa_bwd_workspace_bytes.restype = sz
+        lib.fa_fp8_quantize.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+        lib.fa_fp8_quantize.restype = i
+        lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd_fp8.restype = i
         lib.fa_last_error.argtypes = []
         lib.fa_last_error.restype = ctypes.c_char_p
         lib.fa_splitkv_noalloc_capacity_bytes.argtypes = []
@@ -238,6 +244,65 @@ class _Attention(torch.autograd.Function):
 def attention(q, k, v, causal: bool = False, scale: float | None = None):
     """Differentiable attention: fa_fwd in the forward pass, fa_bwd in the backward."""
     return _Attention.apply(q, k, v, bool(causal), scale)
+
+
+def fp8_quantize(x, transpose: bool = False, out=None, scales=None, stream=None):
+    """E4M3 codes (uint8) and per-128-row-block fp32 scales of x [B, H, N, 128] through
+    ``fa_fp8_quantize``.  transpose=False: codes [B, H, N, 128]; transpose=True (the
+    layout of V for fwd_fp8): codes [B, H, 128, ceil(N/128)*128]."""
+    if not x.is_cuda or x.dim() != 4 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA [B, H, N, d] tensor")
+    B, H, N, d = x.shape
+    nb = (N + 127) // 128
+    shape = (B, H, d, nb * 128) if transpose else (B, H, N, d)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.uint8, device=x.device)
+    elif tuple(out.shape) != shape or out.dtype != torch.uint8 or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous uint8 {shape} tensor")
+    if scales is None:
+        scales = torch.empty((B * H, nb), dtype=torch.float32, device=x.device)
+    elif tuple(scales.shape) != (B * H, nb) or scales.dtype != torch.float32 or not scales.is_contiguous():
+        raise ValueError(f"scales must be a contiguous fp32 {(B * H, nb)} tensor")
+    rc = load_library().fa_fp8_quantize(x.data_ptr(), out.data_ptr(), scales.data_ptr(), B * H, N, d,
+                                        int(bool(transpose)), _dtype_code(x), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fp8_quantize")
+    return out, scales
+
+
+def fwd_fp8(q8, q_scale, k8, k_scale, v8t, v_scale, causal: bool = False, scale: float | None = None,
+            out_dtype=torch.bfloat16, out=None, lse=None, want_lse: bool = True, stream=None):
+    """FP8 attention forward through ``fa_fwd_fp8`` on codes and scales made by
+    fp8_quantize (v8t from the transposed form).  Returns (o, lse)."""
+    for name, t in (("q8", q8), ("k8", k8), ("v8t", v8t)):
+        if not t.is_cuda or t.dtype != torch.uint8 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous uint8 CUDA tensor")
+    B, H, Nq, d = q8.shape
+    Nk = k8.shape[2]
+    if k8.shape != (B, H, Nk, d) or v8t.shape != (B, H, d, (Nk + 127) // 128 * 128):
+        raise ValueError(f"shape mismatch q8{tuple(q8.shape)} k8{tuple(k8.shape)} v8t{tuple(v8t.shape)}")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=out_dtype, device=q8.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q8.device)
+    code = FA_BF16 if out.dtype == torch.bfloat16 else FA_F16
+    rc = load_library().fa_fwd_fp8(q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(),
+                                   v8t.data_ptr(), v_scale.data_ptr(), out.data_ptr(),
+                                   lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d,
+                                   int(bool(causal)), scale, code, _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_fp8")
+    return out, lse
+
+
+def fwd_fp8_from(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Quantize 16-bit q, k, v (fa_fp8_quantize) and run fa_fwd_fp8; returns (o, lse)
+    in q's dtype."""
+    q8, qs = fp8_quantize(q, stream=stream)
+    k8, ks = fp8_quantize(k, stream=stream)
+    v8t, vs = fp8_quantize(v, transpose=True, stream=stream)
+    return fwd_fp8(q8, qs, k8, ks, v8t, vs, causal=causal, scale=scale, out_dtype=q.dtype, stream=stream)
 
 
 def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal: bool = False,

@@ -116,6 +116,19 @@ int make_map_packed(CUtensorMap *map, const void *ptr, bool bf16, int d, int hea
     return r == CUDA_SUCCESS ? FA_OK : cuda_fail("cuTensorMapEncodeTiled", (int)r, nullptr);
 }
 
+// 8-bit tensor [heads][rows][cols] (cols a multiple of 16), boxes of 128 columns x
+// 128 rows x 1 head, 128-byte swizzle; rows and columns past the end read as zero.
+int make_map_u8(CUtensorMap *map, const void *ptr, int cols, int rows, int heads) {
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)cols, (cuuint64_t)rows * cols};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : cuda_fail("cuTensorMapEncodeTiled", (int)r, nullptr);
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int check_common(const void *q, const void *k, const void *v, const void *o, const float *lse, int B, int H,
@@ -348,6 +361,64 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *
                    size_t workspace_bytes, fa_stream_t stream) {
     return fa_fwd_splitkv_gqa(q, k, v, o, lse, B, H, H, Nq, Nk, d, causal, scale, dtype, num_splits, workspace,
                               workspace_bytes, stream);
+}
+
+int fa_fp8_quantize(const void *x, void *x8, float *scales, int BH, int N, int d, int transpose, fa_dtype dtype,
+                    fa_stream_t stream) {
+    if (x == nullptr || x8 == nullptr || scales == nullptr) return FA_ERR_INVALID_ARG;
+    if (BH <= 0 || BH > 65535 || N <= 0 || (transpose != 0 && transpose != 1)) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_F16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned(x, 16) || !aligned(x8, 16) || !aligned(scales, 4)) return FA_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    int rc = dev_state(&st);
+    if (rc != FA_OK) return rc;
+    Fp8QuantArgs a;
+    a.x = x;
+    a.x8 = x8;
+    a.scales = scales;
+    a.N = N;
+    a.num_blocks = (N + 127) / 128;
+    a.ld_t = a.num_blocks * 128;
+    return launch_status("kernel launch",
+                         launch_fp8_quant(dtype == FA_BF16, transpose != 0, a, BH, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fa_fwd_fp8(const void *q8, const float *q_scale, const void *k8, const float *k_scale, const void *v8t,
+               const float *v_scale, void *o, float *lse, int B, int H, int Nq, int Nk, int d, int causal, float scale,
+               fa_dtype out_dtype, fa_stream_t stream) {
+    if (q8 == nullptr || k8 == nullptr || v8t == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
+    if (q_scale == nullptr || k_scale == nullptr || v_scale == nullptr) return FA_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (long long)B * H > 65535) return FA_ERR_INVALID_ARG;
+    if (!(std::isfinite(scale) && scale > 0.f) || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
+    if (out_dtype != FA_F16 && out_dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned(q8, 16) || !aligned(k8, 16) || !aligned(v8t, 16) || !aligned(o, 16)) return FA_ERR_MISALIGNED;
+    if (!aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4)) return FA_ERR_MISALIGNED;
+    if (lse != nullptr && !aligned(lse, 4)) return FA_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    int rc = dev_state(&st);
+    if (rc != FA_OK) return rc;
+    const int BH = B * H;
+    const int nbk = (Nk + 127) / 128;
+    CUtensorMap tq, tk, tv;
+    if ((rc = make_map_u8(&tq, q8, 128, Nq, BH)) != FA_OK || (rc = make_map_u8(&tk, k8, 128, Nk, BH)) != FA_OK ||
+        (rc = make_map_u8(&tv, v8t, nbk * 128, 128, BH)) != FA_OK)
+        return rc;
+    Fp8FwdArgs a;
+    a.o = o;
+    a.lse = lse;
+    a.q_scale = q_scale;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.status = st->status;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.num_m = (Nq + 127) / 128;
+    a.causal = causal;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    return launch_status("kernel launch", launch_fwd_fp8(out_dtype == FA_BF16, tq, tk, tv, a, BH,
+                                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d) {

@@ -79,6 +79,26 @@ struct BwdArgs {
     float scale_log2;  // scale * log2(e)
 };
 
+// FP8 (E4M3) forward: blocks of 128 rows of one head carry one fp32 scale each.
+struct Fp8QuantArgs {
+    const void *x;   // [BH, N, d] 16-bit, d = 128
+    void *x8;        // [BH, N, d] codes, or [BH, d, ld_t] when transposed
+    float *scales;   // [BH, num_blocks]
+    int N, num_blocks;
+    int ld_t;        // row length of the transposed output (num_blocks * 128)
+};
+
+struct Fp8FwdArgs {
+    void *o;               // [BH, Nq, d] 16-bit
+    float *lse;            // [BH, Nq] or nullptr
+    const float *q_scale;  // [BH, num_m]
+    const float *k_scale;  // [BH, ceil(Nk / 128)]
+    const float *v_scale;  // [BH, ceil(Nk / 128)]
+    int *status;
+    int Nq, Nk, num_m, causal;
+    float scale_log2;      // scale * log2(e)
+};
+
 // Each launcher returns the CUDA error of the launch (cudaSuccess when queued).
 cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const FwdArgs &a, int BH, cudaStream_t stream);
@@ -89,6 +109,9 @@ cudaError_t launch_fwd_varlen(int d, bool bf16, const CUtensorMap &tq, const CUt
 cudaError_t launch_splitkv(int d, bool bf16, const CUtensorMap &tk, const CUtensorMap &tv, const SplitArgs &a,
                            cudaStream_t stream);
 cudaError_t launch_combine(int d, bool bf16, const CombineArgs &a, cudaStream_t stream);
+cudaError_t launch_fp8_quant(bool bf16, bool transpose, const Fp8QuantArgs &a, int BH, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(bool bf16_out, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                           const Fp8FwdArgs &a, int BH, cudaStream_t stream);
 // Backward: preprocess (D, lse2, zero dq_acc), the main K/V-block kernel, dQ conversion.
 cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream);

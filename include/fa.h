@@ -262,6 +262,35 @@ FA_API int fa_bwd(const void *q, const void *k, const void *v, const void *o, co
                   fa_dtype dtype, void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
+ * FP8 (E4M3) forward with per-block scales ("Flash Attention (4)" §5.4: both
+ * products in E4M3, block-wise scale factors against underflow).
+ *
+ * fa_fp8_quantize: x [BH, N, d] 16-bit (dtype) to E4M3 codes, one fp32 scale per
+ * block of 128 rows of one head: s = amax / 448 (1 for an all-zero block) and
+ * code = E4M3(x / s) (fp32 division; round to nearest, ties to even; magnitudes
+ * above 448 saturate).  scales is [BH, ceil(N/128)].  transpose = 0 writes x8 as
+ * [BH, N, d] (the layout of q8 and k8); transpose = 1 writes it as
+ * [BH, d, ceil(N/128)*128] with zero codes past N (the layout of v8t).
+ *
+ * fa_fwd_fp8: O and LSE of attention over the dequantized inputs (Q = q8 x
+ * q_scale of each 128-row block, likewise K and V), causal as fa_fwd.  q8, k8:
+ * [B, H, Nq or Nk, d] codes; v8t: [B, H, d, ceil(Nk/128)*128] codes; q_scale
+ * [B*H, ceil(Nq/128)], k_scale and v_scale [B*H, ceil(Nk/128)]; o [B, H, Nq, d] in
+ * out_dtype; lse [B, H, Nq] fp32 or NULL.  Both products run in E4M3 with fp32
+ * accumulation; P is rounded to E4M3 after scaling by 2^7 times the V block's scale
+ * over the head's largest V scale, so its relative rounding error is at most 2^-4
+ * (absolute 2^-10 / that factor below 2^-6).  d must be 128 (FA_ERR_UNSUPPORTED
+ * otherwise).  Errors: FA_ERR_INVALID_ARG for null pointers, non-positive sizes,
+ * B*H > 65535, a bad scale or dtype; FA_ERR_MISALIGNED for code tensors or o not
+ * 16-byte aligned, scales or lse not 4-byte aligned.
+ */
+FA_API int fa_fp8_quantize(const void *x, void *x8, float *scales, int BH, int N, int d, int transpose,
+                           fa_dtype dtype, fa_stream_t stream);
+FA_API int fa_fwd_fp8(const void *q8, const float *q_scale, const void *k8, const float *k_scale, const void *v8t,
+                      const float *v_scale, void *o, float *lse, int B, int H, int Nq, int Nk, int d, int causal,
+                      float scale, fa_dtype out_dtype, fa_stream_t stream);
+
+/*
  * The reason for the last FA_ERR_CUDA returned to the calling thread (the CUDA
  * call that failed and its error name), or "" if there was none.  The string
  * belongs to the library and stays valid until this thread's next call.
