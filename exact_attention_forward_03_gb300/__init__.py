@@ -44,7 +44,7 @@ FA_ERR_SCRATCH_LIMIT = -7
 EXPORTS = ("fa_fwd", "fa_fwd_splitkv", "fa_splitkv_combine", "fa_splitkv_workspace_bytes",
            "fa_splitkv_num_splits", "fa_splitkv_split_len", "fa_get_device_status", "fa_status_string",
            "fa_version", "fa_fwd_splitkv_noalloc", "fa_splitkv_noalloc_capacity_bytes", "fa_fwd_gqa",
-           "fa_fwd_splitkv_gqa", "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace_bytes", "fa_last_error", "fa_fp8_quantize", "fa_fwd_fp8")
+           "fa_fwd_splitkv_gqa", "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace_bytes", "fa_last_error", "fa_fp8_quantize", "fa_fwd_fp8", "fa_selftest_timeout")
 
 _lock = threading.Lock()
 _lib = None
@@ -107,6 +107,8 @@ def load_library(path: str | None = None):
         lib.fa_fp8_quantize.restype = i
         lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_fp8.restype = i
+        lib.fa_selftest_timeout.argtypes = [i, vp]
+        lib.fa_selftest_timeout.restype = i
         lib.fa_last_error.argtypes = []
         lib.fa_last_error.restype = ctypes.c_char_p
         lib.fa_splitkv_noalloc_capacity_bytes.argtypes = []
@@ -432,6 +434,14 @@ def splitkv_combine(o_part, lse_part, dtype=torch.bfloat16, out=None, lse=None, 
     if rc != FA_OK:
         raise FaError(rc, "fa_splitkv_combine")
     return out, lse
+
+
+def selftest_timeout(limit_ms: int = 50, stream=None) -> None:
+    """Launch the timeout self-test kernel (fa_selftest_timeout); read the result
+    with get_device_status()."""
+    rc = load_library().fa_selftest_timeout(int(limit_ms), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_selftest_timeout")
 
 
 def get_device_status(stream=None) -> int:

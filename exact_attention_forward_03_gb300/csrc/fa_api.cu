@@ -492,6 +492,15 @@ int fa_get_device_status(fa_stream_t stream) {
 
 size_t fa_splitkv_noalloc_capacity_bytes(void) { return kNoAllocScratchBytes; }
 
+int fa_selftest_timeout(int limit_ms, fa_stream_t stream) {
+    if (limit_ms < 1 || limit_ms > 10000) return FA_ERR_INVALID_ARG;
+    DeviceState *st = nullptr;
+    int rc = dev_state(&st);
+    if (rc != FA_OK) return rc;
+    return launch_status("kernel launch", launch_selftest_timeout(st->status, limit_ms,
+                                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq,
                            int Nk, int d, int causal, float scale, fa_dtype dtype, int num_splits, fa_stream_t stream) {
     int rc = check_common(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, dtype);

@@ -112,6 +112,8 @@ cudaError_t launch_combine(int d, bool bf16, const CombineArgs &a, cudaStream_t 
 cudaError_t launch_fp8_quant(bool bf16, bool transpose, const Fp8QuantArgs &a, int BH, cudaStream_t stream);
 cudaError_t launch_fwd_fp8(bool bf16_out, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                            const Fp8FwdArgs &a, int BH, cudaStream_t stream);
+// A wait on an mbarrier that never completes, given up after limit_ms.
+cudaError_t launch_selftest_timeout(int *status, int limit_ms, cudaStream_t stream);
 // Backward: preprocess (D, lse2, zero dq_acc), the main K/V-block kernel, dQ conversion.
 cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream);

@@ -291,6 +291,15 @@ FA_API int fa_fwd_fp8(const void *q8, const float *q_scale, const void *k8, cons
                       float scale, fa_dtype out_dtype, fa_stream_t stream);
 
 /*
+ * Self-test of device-side failure reporting: launches one warp that waits on an
+ * mbarrier nothing will complete, gives up after limit_ms (1..10000) exactly as
+ * the attention kernels' bounded waits do, and sets the device status word; the
+ * next fa_get_device_status on that stream returns FA_ERR_DEVICE_TIMEOUT and
+ * clears it.  Nothing faults, traps or hangs; the context stays usable.
+ */
+FA_API int fa_selftest_timeout(int limit_ms, fa_stream_t stream);
+
+/*
  * The reason for the last FA_ERR_CUDA returned to the calling thread (the CUDA
  * call that failed and its error name), or "" if there was none.  The string
  * belongs to the library and stays valid until this thread's next call.

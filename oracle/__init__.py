@@ -236,6 +236,27 @@ def attention_gqa(q, k, v, causal: bool, scale: float, lib=None):
     return o.reshape(B, H, Nq, d), lse.reshape(B, H, Nq)
 
 
+def attention_bwd_gqa(q, k, v, dout, causal: bool, scale: float, lib=None):
+    """Gradients of grouped-query attention ("Lecture 25" §3.3 per query head;
+    "Flash Attention (4)" §5 for the head mapping).  q, dout: [B, H, Nq, d]; k, v:
+    [B, H_kv, Nk, d].  Each query head's gradients are those of plain attention
+    against its group's K/V head; a K/V head's dK, dV are the sums over the query
+    heads that read it.  Returns (dQ [B, H, Nq, d], dK, dV [B, H_kv, Nk, d])."""
+    q64, k64, v64, g64 = to_f64(q), to_f64(k), to_f64(v), to_f64(dout)
+    B, H, Nq, d = q64.shape
+    H_kv, Nk = k64.shape[1], k64.shape[2]
+    if H_kv <= 0 or H % H_kv != 0:
+        raise ValueError("attention_bwd_gqa: H_kv must divide H")
+    group = H // H_kv
+    k_rep = np.repeat(k64, group, axis=1)  # query head h reads K/V head h // group
+    v_rep = np.repeat(v64, group, axis=1)
+    dq, dk_rep, dv_rep = attention_bwd(q64.reshape(B * H, Nq, d), k_rep.reshape(B * H, Nk, d),
+                                       v_rep.reshape(B * H, Nk, d), g64.reshape(B * H, Nq, d), causal, scale, lib=lib)
+    dk = dk_rep.reshape(B, H_kv, group, Nk, d).sum(axis=2)
+    dv = dv_rep.reshape(B, H_kv, group, Nk, d).sum(axis=2)
+    return dq.reshape(B, H, Nq, d), dk, dv
+
+
 def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool, scale: float, lib=None):
     """Exact attention of a packed variable-length batch.  q: [total_q, H, d], k, v:
     [total_k, H_kv, d], cu_seqlens_q/k: num_seqs + 1 token offsets.  Sequence s is

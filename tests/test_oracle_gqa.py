@@ -92,3 +92,38 @@ def test_rejects_a_head_count_that_does_not_divide():
     q = np.zeros((1, 3, 2, 4)); k = np.zeros((1, 2, 2, 4))
     with pytest.raises(ValueError):
         oracle.attention_gqa(q, k, k, False, 1.0)
+
+
+def test_bwd_gqa_finite_differences():
+    """The grouped-query backward is the derivative of the grouped-query forward:
+    central differences of L = sum(O * G) through oracle.attention_gqa."""
+    g = np.random.default_rng(12)
+    B, H, H_kv, Nq, Nk, d = 1, 4, 2, 5, 6, 3
+    q = g.standard_normal((B, H, Nq, d))
+    k = g.standard_normal((B, H_kv, Nk, d))
+    v = g.standard_normal((B, H_kv, Nk, d))
+    G = g.standard_normal((B, H, Nq, d))
+    for causal in (False, True):
+        dq, dk, dv = oracle.attention_bwd_gqa(q, k, v, G, causal, 0.6)
+        for x, got in ((q, dq), (k, dk), (v, dv)):
+            fd = np.zeros_like(x)
+            it = np.nditer(x, flags=["multi_index"])
+            for _ in it:
+                idx = it.multi_index
+                old = x[idx]
+                x[idx] = old + 1e-6
+                op, _ = oracle.attention_gqa(q, k, v, causal, 0.6)
+                x[idx] = old - 1e-6
+                om, _ = oracle.attention_gqa(q, k, v, causal, 0.6)
+                x[idx] = old
+                fd[idx] = ((op - om) * G).sum() / 2e-6
+            assert np.allclose(got, fd, atol=1e-8, rtol=0)
+
+
+def test_bwd_gqa_with_one_query_head_per_kv_head_is_plain_bwd():
+    g = np.random.default_rng(13)
+    q, k, v, G = (g.standard_normal((2, 3, 7, 4)) for _ in range(4))
+    a = oracle.attention_bwd_gqa(q, k, v, G, True, 0.5)
+    b = oracle.attention_bwd(q.reshape(6, 7, 4), k.reshape(6, 7, 4), v.reshape(6, 7, 4), G.reshape(6, 7, 4), True, 0.5)
+    for x, y in zip(a, b):
+        assert np.array_equal(x.reshape(y.shape), y)
