@@ -44,7 +44,7 @@ FA_ERR_SCRATCH_LIMIT = -7
 EXPORTS = ("fa_fwd", "fa_fwd_splitkv", "fa_splitkv_combine", "fa_splitkv_workspace_bytes",
            "fa_splitkv_num_splits", "fa_splitkv_split_len", "fa_get_device_status", "fa_status_string",
            "fa_version", "fa_fwd_splitkv_noalloc", "fa_splitkv_noalloc_capacity_bytes", "fa_fwd_gqa",
-           "fa_fwd_splitkv_gqa", "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace_bytes", "fa_last_error", "fa_fp8_quantize", "fa_fwd_fp8", "fa_selftest_timeout")
+           "fa_fwd_splitkv_gqa", "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace_bytes", "fa_last_error", "fa_fp8_quantize", "fa_fwd_fp8", "fa_selftest_timeout", "fa_bwd_gqa")
 
 _lock = threading.Lock()
 _lib = None
@@ -101,6 +101,8 @@ def load_library(path: str | None = None):
         lib.fa_fwd_varlen.restype = i
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
         lib.fa_bwd.restype = i
+        lib.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, sz, vp]
+        lib.fa_bwd_gqa.restype = i
         lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
         lib.fa_bwd_workspace_bytes.restype = sz
         lib.fa_fp8_quantize.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
@@ -197,9 +199,10 @@ def bwd_workspace_bytes(B, H, Nq, d) -> int:
 
 def bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
         workspace=None, stream=None):
-    """Attention backward through ``fa_bwd``: (dq, dk, dv) for the forward that gave
-    (o, lse) from (q, k, v) with the same causal flag and scale."""
-    B, H, H_kv, Nq, Nk, d = _check_qkv(q, k, v, allow_gqa=False)
+    """Attention backward through ``fa_bwd`` (``fa_bwd_gqa`` when k and v have fewer
+    heads than q): (dq, dk, dv) for the forward that gave (o, lse) from (q, k, v)
+    with the same causal flag and scale."""
+    B, H, H_kv, Nq, Nk, d = _check_qkv(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     for name, t, shape in (("o", o, q.shape), ("dout", dout, q.shape)):
         if not t.is_cuda or t.shape != shape or t.dtype != q.dtype or not t.is_contiguous():
@@ -217,12 +220,12 @@ def bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
     need = bwd_workspace_bytes(B, H, Nq, d)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    rc = load_library().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
-                               lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d,
-                               int(bool(causal)), scale, _dtype_code(q), workspace.data_ptr(),
-                               workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    rc = load_library().fa_bwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                                   lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, H_kv, Nq, Nk, d,
+                                   int(bool(causal)), scale, _dtype_code(q), workspace.data_ptr(),
+                                   workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if rc != FA_OK:
-        raise FaError(rc, "fa_bwd")
+        raise FaError(rc, "fa_bwd_gqa")
     return dq, dk, dv
 
 

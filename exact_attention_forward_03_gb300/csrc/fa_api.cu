@@ -427,11 +427,12 @@ size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d) {
     return align256(rows * d * sizeof(float)) + 2 * align256(rows * sizeof(float));
 }
 
-int fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse, void *dq,
-           void *dk, void *dv, int B, int H, int Nq, int Nk, int d, int causal, float scale, fa_dtype dtype,
-           void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse,
+               void *dq, void *dk, void *dv, int B, int H, int H_kv, int Nq, int Nk, int d, int causal, float scale,
+               fa_dtype dtype, void *workspace, size_t workspace_bytes, fa_stream_t stream) {
     int rc = check_common(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, dtype);
     if (rc != FA_OK) return rc;
+    if (H_kv <= 0 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     if (dout == nullptr || lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
         return FA_ERR_INVALID_ARG;
     if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16)) return FA_ERR_MISALIGNED;
@@ -444,8 +445,8 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const voi
     const int BH = B * H;
     const int Nq_pad = (Nq + kBwdBr - 1) / kBwdBr * kBwdBr;
     CUtensorMap tq, tk, tv, tdo;
-    if (make_map(&tq, q, bf16, d, Nq, BH, kBwdBr) != FA_OK || make_map(&tk, k, bf16, d, Nk, BH, kBwdBc) != FA_OK ||
-        make_map(&tv, v, bf16, d, Nk, BH, kBwdBc) != FA_OK || make_map(&tdo, dout, bf16, d, Nq, BH, kBwdBr) != FA_OK)
+    if (make_map(&tq, q, bf16, d, Nq, BH, kBwdBr) != FA_OK || make_map(&tk, k, bf16, d, Nk, B * H_kv, kBwdBc) != FA_OK ||
+        make_map(&tv, v, bf16, d, Nk, B * H_kv, kBwdBc) != FA_OK || make_map(&tdo, dout, bf16, d, Nq, BH, kBwdBr) != FA_OK)
         return FA_ERR_CUDA;
     const size_t rows = (size_t)BH * Nq_pad;
     BwdArgs a;
@@ -463,11 +464,20 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const voi
     a.Nq = Nq;
     a.Nk = Nk;
     a.Nq_pad = Nq_pad;
+    a.H = H;
+    a.group = H / H_kv;
     a.causal = causal;
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
     cudaError_t e = launch_bwd(d, bf16, tq, tk, tv, tdo, a, reinterpret_cast<cudaStream_t>(stream));
     return launch_status("kernel launch", e);
+}
+
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse, void *dq,
+           void *dk, void *dv, int B, int H, int Nq, int Nk, int d, int causal, float scale, fa_dtype dtype,
+           void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+    return fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, H, Nq, Nk, d, causal, scale, dtype, workspace,
+                      workspace_bytes, stream);
 }
 
 int fa_get_device_status(fa_stream_t stream) {

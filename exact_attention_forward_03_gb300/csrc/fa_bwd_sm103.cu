@@ -8,8 +8,10 @@
 // Three launches:
 //   1. preprocess: D_i, LSE_i * log2(e) (+inf for a row that sees no key and for
 //      the padding rows up to a multiple of 128), and a zeroed fp32 dQ accumulator;
-//   2. main: one CTA per 128-key block and head keeps K_j, V_j and the dK_j, dV_j
-//      accumulators on chip and walks the query blocks that see the block
+//   2. main: one CTA per 128-key block and K/V head keeps K_j, V_j and the dK_j,
+//      dV_j accumulators on chip and walks the query blocks that see the block, of
+//      every query head that reads the K/V head (grouped-query attention sums
+//      those heads' contributions to dK and dV on chip)
 //      ("02 · FA2: parallelism and work partitioning" §5: the K/V block fixed, the
 //      Q blocks in the inner loop, dQ summed across CTAs with atomic adds);
 //   3. dQ = scale * accumulator, rounded to 16 bits.
@@ -146,7 +148,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int k0 = blockIdx.x * kBwdBc;  // first key of this block (block 0 has the most work when causal)
-    const int bh = blockIdx.y;
+    const int bhk = blockIdx.y;          // K/V head (b * H_kv + h_kv)
     const int Nq = args.Nq, Nk = args.Nk, Nq_pad = args.Nq_pad, causal = args.causal;
     const int num_m = (Nq + kBwdBr - 1) / kBwdBr;
     // Query row q sees key k when k <= q + (Nk - Nq) under the causal mask, so the
@@ -156,7 +158,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int first_q = k0 - (Nk - Nq);
         i_start = first_q <= 0 ? 0 : first_q / kBwdBr;
     }
-    const int n = max(0, num_m - i_start);
+    // Step t visits query block i_start + t % n_q of the (t / n_q)-th query head that
+    // reads this K/V head (grouped-query attention: `group` consecutive query heads).
+    const int n_q = max(0, num_m - i_start);
+    const int n = n_q * args.group;
+    const int H_kv = args.H / args.group;
+    const int bh0 = (bhk / H_kv) * args.H + (bhk % H_kv) * args.group;  // first query head of the group
+    auto step_q0 = [&](int t) { return (i_start + t % n_q) * kBwdBr; };
+    auto step_bh = [&](int t) { return bh0 + t / n_q; };
 
     auto bar = [&](int idx) -> uint32_t { return sb + C::kOffBar + 8u * (uint32_t)idx; };
     constexpr int S_ = C::kStages;
@@ -224,15 +233,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             uint32_t pend_q = 0, pend_do = 0, par_q = 0, par_do = 0;
             mbar_arrive_expect_tx(bar(B_KV), 2 * C::kTileBytes);
             for (int b = 0; b < C::kBlocks; ++b) {
-                tma_load_3d(sb + C::kOffK + b * C::kBlockBytes, &tmK, b * 64, k0, bh, bar(B_KV));
-                tma_load_3d(sb + C::kOffV + b * C::kBlockBytes, &tmV, b * 64, k0, bh, bar(B_KV));
+                tma_load_3d(sb + C::kOffK + b * C::kBlockBytes, &tmK, b * 64, k0, bhk, bar(B_KV));
+                tma_load_3d(sb + C::kOffV + b * C::kBlockBytes, &tmV, b * 64, k0, bhk, bar(B_KV));
             }
-            const size_t vec_row = (size_t)bh * Nq_pad;
             bool ok = true;
             for (int t = 0; ok && t < n; ++t) {
                 const int s = t % S_;
                 const uint32_t it = (uint32_t)(t / S_);
-                const int q0 = (i_start + t) * kBwdBr;
+                const int q0 = step_q0(t), bh = step_bh(t);
+                const size_t vec_row = (size_t)bh * Nq_pad;
                 ok = mbar_wait_backoff(bar(B_QEMPTY(s)), (it & 1u) ^ 1u, abort_flag, status, 32);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(B_QFULL(s)), C::kTileBytes + C::kVecBytes);
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(qw * 32) << 16);
         bool ok = true;
         for (int t = 0; t < n; ++t) {
-            const int q0 = (i_start + t) * kBwdBr;
+            const int q0 = step_q0(t), bh = step_bh(t);
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_DQFULL), (uint32_t)t & 1u, abort_flag, status));
             if (!ok) break;
             tc_fence_after();
@@ -429,7 +438,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int t = 0; t < n; ++t) {
             const int s = t % S_;
             const uint32_t pt = (uint32_t)t & 1u;
-            const int q0 = (i_start + t) * kBwdBr;
+            const int q0 = step_q0(t);
             const bool masked = tail_block || (causal && (q0 + (Nk - Nq) < k0 + kBwdBc - 1));
             // ---- P = 2^(S scale log2(e) - LSE log2(e)) for this thread's key and 64 queries
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_QFULL(s)), (uint32_t)(t / S_) & 1u, abort_flag,
@@ -505,7 +514,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // Epilogue: this warp's half of the head dimension of dV_j and dK_j = scale * acc.
             // The tensor-memory loads are warp-collective: every lane takes part, and
             // only lanes whose key exists store.
-            const size_t orow = ((size_t)bh * Nk + j) * D;
+            const size_t orow = ((size_t)bhk * Nk + j) * D;
 #pragma unroll 1
             for (int which = 0; which < 2; ++which) {
                 typename PK::T *dst_row = reinterpret_cast<typename PK::T *>(which == 0 ? args.dv : args.dk) + orow;
@@ -610,7 +619,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, co
     auto kern = fa_bwd_kernel<D, BF16>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)((a.Nk + kBwdBc - 1) / kBwdBc), (unsigned)a.BH, 1);
+    dim3 grid((unsigned)((a.Nk + kBwdBc - 1) / kBwdBc), (unsigned)(a.BH / a.group), 1);
     e = launch_kernel(kern, grid, dim3(kBwdThreads), C::kSmemBytes, stream, tq, tk, tv, tdo, a);
     if (e != cudaSuccess) return e;
     const long long n4 = (long long)a.BH * a.Nq * (D / 4);

@@ -59,7 +59,8 @@ struct CombineArgs {
     long long rows;  // BH * Nq
 };
 
-// Backward: one CTA per 128-key block and head; query blocks of 128 rows.
+// Backward: one CTA per 128-key block and K/V head; query blocks of 128 rows of
+// every query head that reads that K/V head.
 constexpr int kBwdBr = 128;
 constexpr int kBwdBc = 128;
 
@@ -67,13 +68,14 @@ struct BwdArgs {
     const void *o;      // [BH, Nq, d] 16-bit (forward output)
     const void *dout;   // [BH, Nq, d] 16-bit
     const float *lse;   // [BH, Nq] natural-log LSE of the forward
-    void *dk, *dv;      // [BH, Nk, d] 16-bit
+    void *dk, *dv;      // [B * H / group, Nk, d] 16-bit (one per K/V head)
     void *dq;           // [BH, Nq, d] 16-bit
     float *dq_acc;      // [BH, Nq_pad, d] fp32 workspace (zeroed by the preprocess kernel)
     float *lse2;        // [BH, Nq_pad] -LSE * log2(e); -inf for padding and rows that see no key
     float *dvec;        // [BH, Nq_pad] -D_i = -rowsum(dO_i * O_i); 0 for padding
     int *status;
-    int BH, Nq, Nk, Nq_pad;
+    int BH, Nq, Nk, Nq_pad;   // BH = B * H query heads
+    int H, group;             // query heads per batch entry; query heads per K/V head
     int causal;
     float scale;       // softmax scale
     float scale_log2;  // scale * log2(e)

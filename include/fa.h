@@ -257,6 +257,14 @@ FA_API size_t fa_splitkv_noalloc_capacity_bytes(void);
  * workspace.
  */
 FA_API size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d);
+/* Grouped-query form: k, v, dk, dv are [B, H_kv, Nk, d] with H_kv dividing H (query
+ * head h reads K/V head h / (H / H_kv), as in fa_fwd_gqa); a K/V head's dK and dV
+ * sum the contributions of the H / H_kv query heads that read it.  fa_bwd is the
+ * case H_kv = H.  FA_ERR_INVALID_ARG if H_kv does not divide H. */
+FA_API int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                      const float *lse, void *dq, void *dk, void *dv, int B, int H, int H_kv, int Nq, int Nk, int d,
+                      int causal, float scale, fa_dtype dtype, void *workspace, size_t workspace_bytes,
+                      fa_stream_t stream);
 FA_API int fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse,
                   void *dq, void *dk, void *dv, int B, int H, int Nq, int Nk, int d, int causal, float scale,
                   fa_dtype dtype, void *workspace, size_t workspace_bytes, fa_stream_t stream);

@@ -153,7 +153,49 @@ def test_bwd_rejects_bad_arguments(fa):
                            ws.data_ptr(), nbytes, torch.cuda.current_stream().cuda_stream)
     assert lib.fa_bwd(*args(need - 1)) == fa.FA_ERR_WORKSPACE
     assert lib.fa_bwd(*args(need)) == fa.FA_OK
-    with pytest.raises(ValueError):
-        fa.bwd(q, k[:, :1].contiguous(), v[:, :1].contiguous(), o, dout, lse)  # grouped K/V heads
     torch.cuda.synchronize()
     assert fa.get_device_status() == fa.FA_OK
+
+
+GQA = [
+    # B, H, H_kv, Nq, Nk, d, dtype, causal
+    (2, 4, 2, 300, 300, 128, "bf16", True),
+    (1, 8, 1, 257, 513, 64, "f16", False),     # multi-query
+    (1, 6, 3, 520, 200, 128, "bf16", True),    # Nq > Nk
+]
+
+
+@pytest.mark.parametrize("case", GQA, ids=lambda c: "B{}H{}Hkv{}Nq{}Nk{}d{}{}{}".format(*c[:7], "c" if c[7] else ""))
+def test_bwd_gqa(fa, case):
+    """Grouped K/V heads: dK, dV of a K/V head sum its query heads' contributions."""
+    B, H, H_kv, Nq, Nk, d, dtype, causal = case
+    q, _, _ = attn_inputs.make_qkv(B, H, Nq, 1, d, dtype, 500 + Nq, "cuda")
+    _, k, v = attn_inputs.make_qkv(B, H_kv, 1, Nk, d, dtype, 600 + Nk, "cuda")
+    dout = attn_inputs.make_dout(B, H, Nq, d, dtype, 700, "cuda")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fwd(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = fa.bwd(q, k, v, o, dout, lse, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.get_device_status() == fa.FA_OK
+    ref = oracle.attention_bwd_gqa(q, k, v, dout, causal, scale)
+    group = H // H_kv
+    # magnitudes per query head against its K/V head, then summed like the gradients
+    rep = lambda x: _np(x).repeat(group, axis=1).reshape(B * H, -1, d)
+    qn, gn = _np(q).reshape(B * H, Nq, d), _np(dout).reshape(B * H, Nq, d)
+    o_ref, lse_ref = oracle.attention(qn, rep(k), rep(v), causal, scale)
+    mq, mk, mv = grad_magnitudes(qn, rep(k), rep(v), o_ref, gn, lse_ref, causal, scale)
+    mk = mk.reshape(B, H_kv, group, Nk, d).sum(axis=2)
+    mv = mv.reshape(B, H_kv, group, Nk, d).sum(axis=2)
+    floors = _floors(q.dtype, Nq * group, Nk, qn, _np(k), gn, scale)  # dK, dV sum Nq * group terms
+    compare_grads((dq, dk, dv), ref, (mq.reshape(ref[0].shape), mk, mv), floors, q.dtype,
+                  f"bwd gqa {case}")
+
+
+def test_bwd_gqa_autograd(fa):
+    q, _, _ = attn_inputs.make_qkv(1, 4, 200, 1, 64, "bf16", 81, "cuda")
+    _, k, v = attn_inputs.make_qkv(1, 1, 1, 200, 64, "bf16", 82, "cuda")
+    qq, kk, vv = (x.clone().requires_grad_(True) for x in (q, k, v))
+    out = fa.attention(qq, kk, vv, causal=True)
+    out.backward(torch.ones_like(out))
+    torch.cuda.synchronize()
+    assert kk.grad.shape == k.shape and torch.isfinite(kk.grad).all() and torch.isfinite(qq.grad).all()
