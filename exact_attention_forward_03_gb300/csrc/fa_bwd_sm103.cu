@@ -164,8 +164,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int n = n_q * args.group;
     const int H_kv = args.H / args.group;
     const int bh0 = (bhk / H_kv) * args.H + (bhk % H_kv) * args.group;  // first query head of the group
-    auto step_q0 = [&](int t) { return (i_start + t % n_q) * kBwdBr; };
-    auto step_bh = [&](int t) { return bh0 + t / n_q; };
+    // Each role walks the steps with a StepCursor: query block and query head of step t,
+    // advanced by counting (no division in the loops).
+    struct StepCursor {
+        int q0, bh, ti, q0_first, n_q;
+        __device__ __forceinline__ void next() {
+            if (++ti == n_q) {
+                ti = 0;
+                q0 = q0_first;
+                ++bh;
+            } else {
+                q0 += kBwdBr;
+            }
+        }
+    };
+    const StepCursor cursor0{i_start * kBwdBr, bh0, 0, i_start * kBwdBr, n_q};
 
     auto bar = [&](int idx) -> uint32_t { return sb + C::kOffBar + 8u * (uint32_t)idx; };
     constexpr int S_ = C::kStages;
@@ -237,10 +250,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tma_load_3d(sb + C::kOffV + b * C::kBlockBytes, &tmV, b * 64, k0, bhk, bar(B_KV));
             }
             bool ok = true;
-            for (int t = 0; ok && t < n; ++t) {
+            StepCursor cur = cursor0;
+            for (int t = 0; ok && t < n; ++t, cur.next()) {
                 const int s = t % S_;
                 const uint32_t it = (uint32_t)(t / S_);
-                const int q0 = step_q0(t), bh = step_bh(t);
+                const int q0 = cur.q0, bh = cur.bh;
                 const size_t vec_row = (size_t)bh * Nq_pad;
                 ok = mbar_wait_backoff(bar(B_QEMPTY(s)), (it & 1u) ^ 1u, abort_flag, status, 32);
                 if (!ok) break;
@@ -379,8 +393,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int qw = warp & 3;
         const uint32_t lane_base = tmem + ((uint32_t)(qw * 32) << 16);
         bool ok = true;
-        for (int t = 0; t < n; ++t) {
-            const int q0 = step_q0(t), bh = step_bh(t);
+        StepCursor cur = cursor0;
+        for (int t = 0; t < n; ++t, cur.next()) {
+            const int q0 = cur.q0, bh = cur.bh;
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_DQFULL), (uint32_t)t & 1u, abort_flag, status));
             if (!ok) break;
             tc_fence_after();
@@ -435,10 +450,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float sl2 = args.scale_log2;
         float p[64];
         bool ok = true;
-        for (int t = 0; t < n; ++t) {
+        StepCursor cur = cursor0;
+        for (int t = 0; t < n; ++t, cur.next()) {
             const int s = t % S_;
             const uint32_t pt = (uint32_t)t & 1u;
-            const int q0 = step_q0(t);
+            const int q0 = cur.q0;
             const bool masked = tail_block || (causal && (q0 + (Nk - Nq) < k0 + kBwdBc - 1));
             // ---- P = 2^(S scale log2(e) - LSE log2(e)) for this thread's key and 64 queries
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_QFULL(s)), (uint32_t)(t / S_) & 1u, abort_flag,
