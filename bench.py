@@ -409,7 +409,9 @@ def run_fa(args, rank, world, local):
                "unit": "TFLOP/s", "flops_per_call": bflops,
                "roofline": {"bound": "tensor", "achieved": bflops / (bmean * 1e-3) / 1e12, "peak": peaks["bf16_tflops"],
                             "unit": "TFLOP/s", "frac": bflops / (bmean * 1e-3) / 1e12 / peaks["bf16_tflops"],
-                            "traffic": None, "note": "whole call (three launches) timed; FLOPs 2.5x the forward's"}}
+                            "traffic": captured_traffic("fa_bwd_call<128,bf16>", w.name),
+                            "note": "whole call (three launches) timed; FLOPs 2.5x the forward's; traffic = DRAM bytes "
+                                    "of the three launches of one call"}}
         status = fa.get_device_status()
         if status != fa.FA_OK:
             raise RuntimeError(f"device status {status} after the backward")
@@ -442,7 +444,7 @@ def run_fa(args, rank, world, local):
                "value": sum_over_ranks(flops, world) / (max_over_ranks(fmean, world) * 1e-3) / 1e12, "unit": "TFLOP/s",
                "quantize_ms_per_call": statistics.mean(qms),
                "roofline": {"bound": "tensor", "achieved": fach, "peak": fpeak, "unit": "TFLOP/s", "frac": fach / fpeak,
-                            "traffic": None,
+                            "traffic": captured_traffic("fa_fwd_fp8_kernel<bf16>", w.name),
                             "note": "inputs quantized beforehand (fa_fp8_quantize of Q, K, V timed separately as "
                                     "quantize_ms_per_call); peak = 2 x measured bf16 (the E4M3/bf16 nominal ratio)"}}
         del q8, k8, v8t, o8
