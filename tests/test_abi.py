@@ -97,3 +97,32 @@ def test_python_binding_refuses_cpu_tensors():
     q = torch.zeros(1, 1, 8, 64, dtype=torch.float16)
     with pytest.raises(ValueError):
         fa.fwd(q, q, q)
+
+
+def test_backward_and_fp8_validation_without_gpu(lib):
+    """Argument checks of fa_bwd, fa_bwd_gqa, fa_fp8_quantize, fa_fwd_fp8 and the
+    self-test run before any CUDA call."""
+    p = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    ws = 1 << 30
+    b = lib.fa_bwd
+    assert b(p, p, p, p, None, p, p, p, p, 1, 2, 8, 8, 128, 0, 0.1, 1, p, ws, None) == -1    # null dout
+    assert b(p, p, p, p, p, None, p, p, p, 1, 2, 8, 8, 128, 0, 0.1, 1, p, ws, None) == -1    # null lse
+    assert b(p, p, p, p, p, p, p, p, p, 1, 2, 8, 8, 96, 0, 0.1, 1, p, ws, None) == -2       # d = 96
+    assert b(p, p, p, p, odd, p, p, p, p, 1, 2, 8, 8, 128, 0, 0.1, 1, p, ws, None) == -3     # dout misaligned
+    assert b(p, p, p, p, p, p, p, p, p, 1, 2, 8, 8, 128, 0, 0.1, 1, None, ws, None) == -4   # no workspace
+    need = lib.fa_bwd_workspace_bytes(1, 2, 8, 128)
+    assert need == 2 * 128 * 128 * 4 + 2 * 1024
+    assert b(p, p, p, p, p, p, p, p, p, 1, 2, 8, 8, 128, 0, 0.1, 1, p, need - 1, None) == -4  # short workspace
+    g = lib.fa_bwd_gqa
+    assert g(p, p, p, p, p, p, p, p, p, 1, 6, 4, 8, 8, 128, 0, 0.1, 1, p, ws, None) == -1   # 6 % 4 != 0
+    q = lib.fa_fp8_quantize
+    assert q(None, p, p, 4, 128, 128, 0, 1, None) == -1
+    assert q(p, p, p, 4, 128, 64, 0, 1, None) == -2      # d = 64
+    assert q(p, p, p, 4, 128, 128, 2, 1, None) == -1     # transpose flag
+    assert q(odd, p, p, 4, 128, 128, 0, 1, None) == -3
+    f = lib.fa_fwd_fp8
+    assert f(p, p, p, p, p, p, p, None, 1, 2, 8, 8, 64, 0, 0.1, 1, None) == -2       # d = 64
+    assert f(p, None, p, p, p, p, p, None, 1, 2, 8, 8, 128, 0, 0.1, 1, None) == -1   # null q_scale
+    assert f(p, p, p, p, odd, p, p, None, 1, 2, 8, 8, 128, 0, 0.1, 1, None) == -3    # v8t misaligned
+    assert lib.fa_selftest_timeout(0, None) == -1
