@@ -17,30 +17,31 @@
  *   LSE_i = m_i + ln l_i        (natural log of the scaled scores)
  *
  * Sources:
- *  - "Lecture 25: why attention needs no intermediate matrix" (page 2),
+ *  - "Lecture 25: why attention needs no intermediate matrix",
  *    §1.1 (standard attention O = softmax(QK^T/sqrt(d)) V) and §2.1 (safe
  *    softmax: subtract the row max, exponentiate, sum, divide).
- *  - "6.2 FlashAttention V2 explained" (page 4), §5.1 (causal mask: -inf
+ *  - "6.2 FlashAttention V2 explained", §5.1 (causal mask: -inf
  *    added before the softmax so row i sees only j <= i) and §6 (the forward
  *    algorithm and its L = m + log(l) output).
- *  - "02 · FA2: parallelism and work partitioning" (page 3), §4 (the causal
+ *  - "02 · FA2: parallelism and work partitioning", §4 (the causal
  *    KV-block bound carries the offset seqlen_k - seqlen_q, i.e. the
  *    diagonal is aligned to the bottom-right corner when Nq != Nk).
  *  - Fully masked rows (possible only when causal and Nq > Nk) give O = 0 and
- *    LSE = -inf: the official FA2 epilogue quoted on page 1 ("Flash Attention
- *    (4) v2.1 forward", §3.5) guards l == 0 by using 1 instead of 1/l, which
+ *    LSE = -inf: the official FA2 epilogue quoted in "Flash Attention (4) v2.1
+ *    forward", §3.5, guards l == 0 by using 1 instead of 1/l, which
  *    leaves the zero accumulator as the output.
  *
  * The backward (oracle_attn_bwd, at the end of this file) is the chain rule of
  * this definition.
  *
  * Two further modes exist only to check invariants of the method:
- *  - oracle_attn_tiled: the page-4 §6 online-softmax loop in fp64, over KV
- *    tiles of a caller-chosen width (with page 1 §2.5's rule that a running
+ *  - oracle_attn_tiled: the online-softmax loop of "6.2 FlashAttention V2
+ *    explained" §6 in fp64, over KV tiles of a caller-chosen width (with the
+ *    rule of "Flash Attention (4)" §2.5 that a running
  *    max of -inf is replaced by 0 before it is subtracted);
  *  - oracle_attn_split_partials + oracle_combine: the split-KV partial
  *    (O_s, LSE_s) per contiguous key range and their LSE-weighted merge
- *    (page 3 §2, "decode / split-KV").
+ *    ("02 · FA2" §2, "decode / split-KV").
  *
  * Every row is independent; rows may run on several OpenMP threads, which
  * changes no arithmetic inside a row.

@@ -28,7 +28,7 @@ def pin_two_key_closed_form(lib):
     """d = 1, two keys: O = sigmoid(s0 - s1) v0 + sigmoid(s1 - s0) v1, LSE = log(e^s0 + e^s1).
 
     Softmax of two scores is the logistic function of their difference
-    ("Lecture 25", §2.1 safe softmax; page 4 §6 L = m + log l).
+    ("Lecture 25", §2.1 safe softmax; "6.2 FlashAttention V2 explained" §6: L = m + log l).
     """
     for (qv, k0, k1, v0, v1, sc) in [(1.0, 0.5, -1.5, 2.0, -3.0, 0.7), (-2.0, 1.0, 3.0, 0.25, 4.0, 1.0),
                                      (0.3, 0.0, 0.0, 1.0, 5.0, 2.0)]:
@@ -48,7 +48,7 @@ def pin_zero_query_uniform(lib):
     """Q = 0 makes every score 0: softmax is uniform.
 
     Non-causal: O_i = mean_j V_j, LSE_i = ln Nk.  Causal (Nq = Nk): O_i is the
-    prefix mean of V_0..V_i and LSE_i = ln(i + 1) (page 4 §5.1: row i sees j <= i).
+    prefix mean of V_0..V_i and LSE_i = ln(i + 1) ("6.2 FlashAttention V2 explained" §5.1: row i sees j <= i).
     """
     BH, N, d = 2, 9, 5
     q = np.zeros((BH, N, d))
@@ -192,7 +192,7 @@ def pin_fully_masked_rows(lib):
 
 
 def pin_tiled_equals_full(lib):
-    """Page 4 §6 online-softmax loop over KV tiles equals the full softmax (Bc in {1, 7, 64, 128, N})."""
+    """The online-softmax loop of "6.2 FlashAttention V2 explained" §6 over KV tiles equals the full softmax (Bc in {1, 7, 64, 128, N})."""
     for causal, (Nq, Nk) in [(False, (70, 150)), (True, (150, 150)), (True, (40, 150)), (True, (20, 9))]:
         BH, d = 2, 8
         q = _rand((BH, Nq, d), 23, 1.5)
@@ -210,7 +210,7 @@ def pin_tiled_equals_full(lib):
 def pin_tiled_growing_max(lib):
     """Row max that rises in a later tile (k_j grows with j): the l * alpha rescale matters.
 
-    Page 1 §2.5 reports a first version that skipped the rescale of l and was
+    "Flash Attention (4)" §2.5 reports a first version that skipped the rescale of l and was
     caught only by a mismatch; here the tiled loop must still equal the full softmax.
     """
     Nk, d = 96, 4
@@ -223,7 +223,7 @@ def pin_tiled_growing_max(lib):
 
 
 def pin_split_combine_equals_full(lib):
-    """Split-KV partials merged by LSE weights equal the full result (page 3 §2, decode / split-KV).
+    """Split-KV partials merged by LSE weights equal the full result ("02 · FA2" §2, decode / split-KV).
 
     Includes more splits than keys, so some partials are empty (LSE_s = -inf).
     """
