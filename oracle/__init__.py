@@ -146,7 +146,8 @@ def attention_bwd(q, k, v, dout, causal: bool, scale: float, lib=None):
 
 
 def attention_tiled(q, k, v, causal: bool, scale: float, Br: int, Bc: int, lib=None):
-    """The page-4 online-softmax loop in fp64 (for the tiled == full invariant)."""
+    """The online-softmax loop of "6.2 FlashAttention V2 explained" §6 in fp64 (for the
+    tiled == full invariant)."""
     lib = lib or load()
     q, k, v = to_f64(q), to_f64(k), to_f64(v)
     lead = q.shape[:-2]

@@ -187,7 +187,8 @@ int oracle_attn_rows(const double *q_rows, const int64_t *row_index, const int64
 }
 
 /*
- * The page-4 §6 forward loop in fp64: rows in blocks of Br, keys in tiles of Bc,
+ * The forward loop of "6.2 FlashAttention V2 explained" §6 in fp64: rows in
+ * blocks of Br, keys in tiles of Bc,
  * running (m, l, O~) per row, deferred 1/l, L = m + ln l.  The causal KV bound
  * is the block's last allowed key (with the Nk - Nq offset).  Exists to show
  * that the tiled online softmax equals the full softmax.
