@@ -283,6 +283,28 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool, scale: f
     return o, lse
 
 
+def attention_bwd_varlen(q, k, v, dout, cu_seqlens_q, cu_seqlens_k, causal: bool, scale: float, lib=None):
+    """Gradients of a packed variable-length batch (layouts as attention_varlen; dout
+    like q): every sequence is its own problem (attention_bwd_gqa on its tokens), and
+    keys of a sequence with no query rows get zero gradients.
+    Returns (dQ [total_q, H, d], dK, dV [total_k, H_kv, d])."""
+    q64, k64, v64, g64 = to_f64(q), to_f64(k), to_f64(v), to_f64(dout)
+    cq = [int(x) for x in np.asarray(to_f64(cu_seqlens_q))]
+    ck = [int(x) for x in np.asarray(to_f64(cu_seqlens_k))]
+    dq, dk, dv = np.zeros_like(q64), np.zeros_like(k64), np.zeros_like(v64)
+    tr = lambda x: np.ascontiguousarray(x.transpose(1, 0, 2))[None]
+    for s in range(len(cq) - 1):
+        q_s, g_s = q64[cq[s]:cq[s + 1]], g64[cq[s]:cq[s + 1]]
+        k_s, v_s = k64[ck[s]:ck[s + 1]], v64[ck[s]:ck[s + 1]]
+        if q_s.shape[0] == 0 or k_s.shape[0] == 0:
+            continue
+        a, b, c = attention_bwd_gqa(tr(q_s), tr(k_s), tr(v_s), tr(g_s), causal, scale, lib=lib)
+        dq[cq[s]:cq[s + 1]] = a[0].transpose(1, 0, 2)
+        dk[ck[s]:ck[s + 1]] = b[0].transpose(1, 0, 2)
+        dv[ck[s]:ck[s + 1]] = c[0].transpose(1, 0, 2)
+    return dq, dk, dv
+
+
 def sampled_rows(q, k, v, pairs, causal: bool, scale: float, heads_per_batch: int = 16):
     """Oracle values for the (bh, row) pairs of ``[B, H, N, d]`` tensors (any device).
 

@@ -65,3 +65,44 @@ def test_a_sequence_never_sees_its_neighbours():
     np.testing.assert_array_equal(o1[5:12], o2[5:12])   # the middle sequence is untouched
     np.testing.assert_array_equal(l1[:, 5:12], l2[:, 5:12])
     assert np.abs(o1[:5] - o2[:5]).max() > 1e-3 and np.abs(o1[12:] - o2[12:]).max() > 1e-3
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_varlen_equal_lengths_are_a_dense_batch(causal):
+    g = np.random.default_rng(21)
+    B, H, N, d = 3, 2, 7, 4
+    q, k, v, G = (g.standard_normal((B, H, N, d)) for _ in range(4))
+    dense = oracle.attention_bwd(q.reshape(B * H, N, d), k.reshape(B * H, N, d), v.reshape(B * H, N, d),
+                                 G.reshape(B * H, N, d), causal, 0.3)
+    pack = lambda x: np.ascontiguousarray(x.transpose(0, 2, 1, 3).reshape(B * N, H, d))
+    cu = [b * N for b in range(B + 1)]
+    got = oracle.attention_bwd_varlen(pack(q), pack(k), pack(v), pack(G), cu, cu, causal, 0.3)
+    for x, y in zip(got, dense):
+        np.testing.assert_allclose(x, pack(y.reshape(B, H, N, d)), rtol=0, atol=1e-12)
+
+
+def test_bwd_varlen_finite_differences_with_an_empty_and_a_keyless_sequence():
+    """Central differences of L = sum(O * G) through oracle.attention_varlen."""
+    g = np.random.default_rng(22)
+    cu_q = [0, 3, 3, 6]      # lengths 3, 0, 3
+    cu_k = [0, 4, 6, 6]      # lengths 4, 2, 0 (the third sequence's rows see no key)
+    H, H_kv, d = 2, 1, 3
+    q = g.standard_normal((cu_q[-1], H, d))
+    k = g.standard_normal((cu_k[-1], H_kv, d))
+    v = g.standard_normal((cu_k[-1], H_kv, d))
+    G = g.standard_normal((cu_q[-1], H, d))
+    for causal in (False, True):
+        got = oracle.attention_bwd_varlen(q, k, v, G, cu_q, cu_k, causal, 0.7)
+        for x, gx in zip((q, k, v), got):
+            fd = np.zeros_like(x)
+            it = np.nditer(x, flags=["multi_index"])
+            for _ in it:
+                idx = it.multi_index
+                old = x[idx]
+                x[idx] = old + 1e-6
+                op, _ = oracle.attention_varlen(q, k, v, cu_q, cu_k, causal, 0.7)
+                x[idx] = old - 1e-6
+                om, _ = oracle.attention_varlen(q, k, v, cu_q, cu_k, causal, 0.7)
+                x[idx] = old
+                fd[idx] = ((op - om) * G).sum() / 2e-6
+            np.testing.assert_allclose(gx, fd, rtol=0, atol=1e-8)
