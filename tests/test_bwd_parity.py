@@ -114,6 +114,25 @@ def test_bwd_full_size_invariants_and_one_head():
     compare_grads((dq[b, h], dk[b, h], dv[b, h]), ref, mags, (0.0, 0.0, 0.0), torch.bfloat16, "bwd full-size head")
 
 
+def test_bwd_full_size_noncausal_one_head(fa):
+    """B=2, H=32, N=8192, d=128, bf16 without the mask: one head element-wise."""
+    B, H, N, d = 2, 32, 8192, 128
+    q, k, v = attn_inputs.make_qkv(B, H, N, N, d, "bf16", 1100, "cuda")
+    dout = attn_inputs.make_dout(B, H, N, d, "bf16", 1100, "cuda")
+    o, lse = fa.fwd(q, k, v, causal=False)
+    dq, dk, dv = fa.bwd(q, k, v, o, dout, lse, causal=False)
+    torch.cuda.synchronize()
+    assert fa.get_device_status() == fa.FA_OK
+    b, h = 0, 7
+    qn, kn, vn, gn = (_np(x[b, h]).reshape(1, N, d) for x in (q, k, v, dout))
+    scale = 1.0 / math.sqrt(d)
+    ref = oracle.attention_bwd(qn, kn, vn, gn, False, scale)
+    o_ref, lse_ref = oracle.attention(qn, kn, vn, False, scale)
+    mags = grad_magnitudes(qn, kn, vn, o_ref, gn, lse_ref, False, scale)
+    compare_grads((dq[b, h], dk[b, h], dv[b, h]), ref, mags, (0.0, 0.0, 0.0), torch.bfloat16,
+                  "bwd full-size non-causal head")
+
+
 def test_dk_dv_deterministic_dq_close(fa):
     q, k, v = attn_inputs.make_qkv(1, 4, 700, 700, 128, "bf16", 77, "cuda")
     dout = attn_inputs.make_dout(1, 4, 700, 128, "bf16", 77, "cuda")

@@ -147,3 +147,34 @@ def test_fp8_rejects_bad_arguments(fa):
         fa.fp8_quantize(q)
     assert e.value.code == fa.FA_ERR_UNSUPPORTED
     assert fa.get_device_status() == fa.FA_OK
+
+
+def test_fwd_fp8_full_size_one_head(fa):
+    """B=2, H=32, N=8192, d=128, causal (the benchmarked FP8 launch): the codes of one
+    head bit for bit and that head's output element-wise within the bound above."""
+    B, H, N, d = 2, 32, 8192, 128
+    w = attn_inputs.WORKLOADS["b2h32_n8192_d128_bf16_causal"]
+    q, k, v = attn_inputs.make_workload(w, "cuda")
+    q8, qs = fa.fp8_quantize(q)
+    k8, ks = fa.fp8_quantize(k)
+    v8t, vs = fa.fp8_quantize(v, transpose=True)
+    o, lse = fa.fwd_fp8(q8, qs, k8, ks, v8t, vs, causal=True)
+    torch.cuda.synchronize()
+    assert fa.get_device_status() == fa.FA_OK
+    b, h = 1, 30
+    bh = b * H + h
+    qr, kr, vr = (x[b, h].reshape(1, N, d).cpu() for x in (q, k, v))
+    rq8, rqs = fp8.quantize_blocks(qr)
+    rk8, rks = fp8.quantize_blocks(kr)
+    rv8, rvs = fp8.quantize_blocks(vr)
+    assert np.array_equal(q8[b, h].cpu().numpy(), rq8[0]) and np.array_equal(qs[bh].cpu().numpy(), rqs[0])
+    assert np.array_equal(k8[b, h].cpu().numpy(), rk8[0]) and np.array_equal(ks[bh].cpu().numpy(), rks[0])
+    assert np.array_equal(v8t[b, h].cpu().numpy().T, rv8[0]) and np.array_equal(vs[bh].cpu().numpy(), rvs[0])
+    scale = 1.0 / math.sqrt(d)
+    o_ref, lse_ref = fp8.attention_fp8(rq8, rqs, rk8, rks, rv8, rvs, True, scale)
+    tol = _fp8_tolerance(fp8.dequantize_blocks(rq8, rqs), fp8.dequantize_blocks(rk8, rks),
+                         fp8.dequantize_blocks(rv8, rvs), rqs, rks, rvs.astype(np.float64), True, scale, o_ref,
+                         torch.bfloat16)
+    err = np.abs(_np(o[b, h]).reshape(o_ref.shape) - o_ref)
+    assert (err <= tol).all(), f"{int((err > tol).sum())} elements out of tolerance"
+    assert np.abs(_np(lse[b, h]) - lse_ref[0]).max() <= 1e-3
