@@ -44,7 +44,8 @@ FA_ERR_SCRATCH_LIMIT = -7
 EXPORTS = ("fa_fwd", "fa_fwd_splitkv", "fa_splitkv_combine", "fa_splitkv_workspace_bytes",
            "fa_splitkv_num_splits", "fa_splitkv_split_len", "fa_get_device_status", "fa_status_string",
            "fa_version", "fa_fwd_splitkv_noalloc", "fa_splitkv_noalloc_capacity_bytes", "fa_fwd_gqa",
-           "fa_fwd_splitkv_gqa", "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace_bytes", "fa_last_error", "fa_fp8_quantize", "fa_fwd_fp8", "fa_selftest_timeout", "fa_bwd_gqa")
+           "fa_fwd_splitkv_gqa", "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace_bytes", "fa_last_error", "fa_fp8_quantize", "fa_fwd_fp8", "fa_selftest_timeout", "fa_bwd_gqa",
+           "fa_bwd_varlen", "fa_bwd_varlen_workspace_bytes")
 
 _lock = threading.Lock()
 _lib = None
@@ -105,6 +106,11 @@ def load_library(path: str | None = None):
         lib.fa_bwd_gqa.restype = i
         lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
         lib.fa_bwd_workspace_bytes.restype = sz
+        lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp,
+                                      sz, vp]
+        lib.fa_bwd_varlen.restype = i
+        lib.fa_bwd_varlen_workspace_bytes.argtypes = [i, i, i, i]
+        lib.fa_bwd_varlen_workspace_bytes.restype = sz
         lib.fa_fp8_quantize.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
         lib.fa_fp8_quantize.restype = i
         lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
@@ -347,6 +353,57 @@ def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal: b
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_varlen")
     return out, lse
+
+
+def bwd_varlen_workspace_bytes(num_seqs, total_q, H, d) -> int:
+    return int(load_library().fa_bwd_varlen_workspace_bytes(num_seqs, total_q, H, d))
+
+
+def bwd_varlen(q, k, v, o, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_k: int, causal: bool = False,
+               scale: float | None = None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward of a variable-length (packed) batch through ``fa_bwd_varlen``:
+    (dq [total_q, H, d], dk, dv [total_k, H_kv, d]) for the ``fwd_varlen`` call that
+    gave (o, lse [H, total_q]).  ``max_seqlen_k`` must bound every sequence's key count."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        if not t.is_cuda or t.dim() != 3 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA [tokens, heads, d] tensor")
+    if not (q.dtype == k.dtype == v.dtype == o.dtype == dout.dtype):
+        raise TypeError("q, k, v, o and dout must share one dtype")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if not t.is_cuda or t.dtype != torch.int32 or t.dim() != 1 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA vector")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold num_seqs + 1 offsets")
+    total_q, H, d = q.shape
+    total_k, H_kv = k.shape[0], k.shape[1]
+    if v.shape != k.shape or k.shape[2] != d or H_kv <= 0 or H % H_kv != 0:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("o and dout must have q's shape")
+    if lse.shape != (H, total_q) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [H, total_q] tensor")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    outs = []
+    for name, t, like in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if t is None:
+            t = torch.empty_like(like)
+        elif t.shape != like.shape or t.dtype != like.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must match its input")
+        outs.append(t)
+    dq, dk, dv = outs
+    num_seqs = cu_seqlens_q.numel() - 1
+    need = bwd_varlen_workspace_bytes(num_seqs, total_q, H, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    rc = load_library().fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                                      lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                      cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), num_seqs, int(max_seqlen_k),
+                                      total_q, total_k, H, H_kv, d, int(bool(causal)), scale, _dtype_code(q),
+                                      workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                      _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_varlen")
+    return dq, dk, dv
 
 
 def splitkv_num_splits(B, H, Nq, Nk, d) -> int:

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdio>
 #include <cstdint>
@@ -449,7 +450,7 @@ int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const
         make_map(&tv, v, bf16, d, Nk, B * H_kv, kBwdBc) != FA_OK || make_map(&tdo, dout, bf16, d, Nq, BH, kBwdBr) != FA_OK)
         return FA_ERR_CUDA;
     const size_t rows = (size_t)BH * Nq_pad;
-    BwdArgs a;
+    BwdArgs a{};
     a.o = o;
     a.dout = dout;
     a.lse = lse;
@@ -470,6 +471,78 @@ int fa_bwd_gqa(const void *q, const void *k, const void *v, const void *o, const
     a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
     cudaError_t e = launch_bwd(d, bf16, tq, tk, tv, tdo, a, reinterpret_cast<cudaStream_t>(stream));
+    return launch_status("kernel launch", e);
+}
+
+// Workspace rows per head of a variable-length backward: room for every sequence
+// to start on a multiple of 128 rows (sum of ceil(len / 128) * 128 over the
+// sequences is at most 128 (ceil(total_q / 128) + num_seqs)).
+static size_t varlen_rows_pad(int num_seqs, int total_q) {
+    return (size_t)kBwdBr * ((size_t)(total_q + kBwdBr - 1) / kBwdBr + (size_t)num_seqs);
+}
+
+size_t fa_bwd_varlen_workspace_bytes(int num_seqs, int total_q, int H, int d) {
+    if (num_seqs <= 0 || total_q <= 0 || H <= 0 || (d != 64 && d != 128)) return 0;
+    const size_t rows = (size_t)H * varlen_rows_pad(num_seqs, total_q);
+    return align256((size_t)(num_seqs + 1) * sizeof(int)) + align256(rows * d * sizeof(float)) +
+           2 * align256(rows * sizeof(float));
+}
+
+int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse,
+                  void *dq, void *dk, void *dv, const int *cu_seqlens_q, const int *cu_seqlens_k, int num_seqs,
+                  int max_seqlen_k, int total_q, int total_k, int H, int H_kv, int d, int causal, float scale,
+                  fa_dtype dtype, void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+    int rc = check_common(q, k, v, o, lse, 1, H, total_q, total_k, d, causal, scale, dtype);
+    if (rc != FA_OK) return rc;
+    if (dout == nullptr || lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr) return FA_ERR_INVALID_ARG;
+    if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return FA_ERR_INVALID_ARG;
+    if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16)) return FA_ERR_MISALIGNED;
+    if (!aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4)) return FA_ERR_MISALIGNED;
+    if (num_seqs <= 0 || max_seqlen_k <= 0 || max_seqlen_k > total_k) return FA_ERR_INVALID_ARG;
+    if (H_kv <= 0 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
+    if ((long long)num_seqs * H_kv > 65535) return FA_ERR_INVALID_ARG;  // grid.y limit
+    if ((long long)H * (long long)varlen_rows_pad(num_seqs, total_q) > INT_MAX) return FA_ERR_INVALID_ARG;
+    const size_t need = fa_bwd_varlen_workspace_bytes(num_seqs, total_q, H, d);
+    if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    DeviceState *st = nullptr;
+    if ((rc = dev_state(&st)) != FA_OK) return rc;
+    const bool bf16 = dtype == FA_BF16;
+    CUtensorMap tq, tk, tv, tdo;
+    if (make_map_packed(&tq, q, bf16, d, H, total_q, kBwdBr) != FA_OK ||
+        make_map_packed(&tk, k, bf16, d, H_kv, total_k, kBwdBc) != FA_OK ||
+        make_map_packed(&tv, v, bf16, d, H_kv, total_k, kBwdBc) != FA_OK ||
+        make_map_packed(&tdo, dout, bf16, d, H, total_q, kBwdBr) != FA_OK)
+        return FA_ERR_CUDA;
+    const size_t rows_pad = varlen_rows_pad(num_seqs, total_q);
+    const size_t rows = (size_t)H * rows_pad;
+    char *ws = static_cast<char *>(workspace);
+    BwdArgs a{};
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.dk = dk;
+    a.dv = dv;
+    a.dq = dq;
+    a.row_off = reinterpret_cast<int *>(ws);
+    ws += align256((size_t)(num_seqs + 1) * sizeof(int));
+    a.dq_acc = reinterpret_cast<float *>(ws);
+    ws += align256(rows * d * sizeof(float));
+    a.lse2 = reinterpret_cast<float *>(ws);
+    ws += align256(rows * sizeof(float));
+    a.dvec = reinterpret_cast<float *>(ws);
+    a.status = st->status;
+    a.BH = H;  // query heads per token
+    a.H = H;
+    a.group = H / H_kv;
+    a.causal = causal;
+    a.scale = scale;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.cu_q = cu_seqlens_q;
+    a.cu_k = cu_seqlens_k;
+    a.num_seqs = num_seqs;
+    a.total_q = total_q;
+    a.rows_pad = (int)rows_pad;
+    cudaError_t e = launch_bwd_varlen(d, bf16, tq, tk, tv, tdo, a, max_seqlen_k, reinterpret_cast<cudaStream_t>(stream));
     return launch_status("kernel launch", e);
 }
 

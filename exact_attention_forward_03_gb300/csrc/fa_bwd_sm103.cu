@@ -128,7 +128,14 @@ __device__ __forceinline__ void bwd_p_chunk(const uint32_t (&sv)[32], const floa
     }
 }
 
-template <int D, bool BF16>
+// VARLEN: a packed variable-length batch.  blockIdx.y = sequence * H_kv + K/V head;
+// q, o, dO are [total_q, H, d], k, v, dK, dV are [total_k, H_kv, d] (tensor maps
+// indexed by column, head, token), and sequence s spans tokens [cu_q[s], cu_q[s+1])
+// of q and [cu_k[s], cu_k[s+1]) of k and v.  A query block may run past its
+// sequence into the next one's tokens: those rows' padded LSE entries are -inf, so
+// they get P = 0 and add nothing; keys past the sequence are masked like a ragged
+// K tail.  A CTA whose key block lies past its sequence's keys leaves at entry.
+template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -148,8 +155,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int k0 = blockIdx.x * kBwdBc;  // first key of this block (block 0 has the most work when causal)
-    const int bhk = blockIdx.y;          // K/V head (b * H_kv + h_kv)
-    const int Nq = args.Nq, Nk = args.Nk, Nq_pad = args.Nq_pad, causal = args.causal;
+    const int causal = args.causal;
+    const int H_kv = args.H / args.group;
+    int Nq, Nk, bhk, bh0, ld_rows, seq_off, q_tok = 0, k_tok = 0;
+    if constexpr (VARLEN) {
+        const int seq = blockIdx.y / H_kv;
+        bhk = blockIdx.y % H_kv;               // K/V head within a token
+        q_tok = args.cu_q[seq];
+        k_tok = args.cu_k[seq];
+        Nq = args.cu_q[seq + 1] - q_tok;
+        Nk = args.cu_k[seq + 1] - k_tok;
+        bh0 = bhk * args.group;                // first query head (within a token) of the group
+        ld_rows = args.rows_pad;               // workspace rows per head
+        seq_off = args.row_off[seq];           // this sequence's first workspace row
+        if (k0 >= Nk) return;                  // the whole CTA: nothing has been touched yet
+    } else {
+        bhk = blockIdx.y;                      // K/V head (b * H_kv + h_kv)
+        Nq = args.Nq;
+        Nk = args.Nk;
+        bh0 = (bhk / H_kv) * args.H + (bhk % H_kv) * args.group;  // first query head of the group
+        ld_rows = args.Nq_pad;
+        seq_off = 0;
+    }
+    // The query rows of head h (global for dense, within a token for VARLEN) and block
+    // q0 sit at workspace rows h * ld_rows + seq_off + q0 ... (vectors and dQ accumulator).
     const int num_m = (Nq + kBwdBr - 1) / kBwdBr;
     // Query row q sees key k when k <= q + (Nk - Nq) under the causal mask, so the
     // first query block with a row that sees key k0 starts at row k0 - (Nk - Nq).
@@ -162,8 +191,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // reads this K/V head (grouped-query attention: `group` consecutive query heads).
     const int n_q = max(0, num_m - i_start);
     const int n = n_q * args.group;
-    const int H_kv = args.H / args.group;
-    const int bh0 = (bhk / H_kv) * args.H + (bhk % H_kv) * args.group;  // first query head of the group
     // Each role walks the steps with a StepCursor: query block and query head of step t,
     // advanced by counting (no division in the loops).
     struct StepCursor {
@@ -246,8 +273,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             uint32_t pend_q = 0, pend_do = 0, par_q = 0, par_do = 0;
             mbar_arrive_expect_tx(bar(B_KV), 2 * C::kTileBytes);
             for (int b = 0; b < C::kBlocks; ++b) {
-                tma_load_3d(sb + C::kOffK + b * C::kBlockBytes, &tmK, b * 64, k0, bhk, bar(B_KV));
-                tma_load_3d(sb + C::kOffV + b * C::kBlockBytes, &tmV, b * 64, k0, bhk, bar(B_KV));
+                if constexpr (VARLEN) {
+                    tma_load_3d(sb + C::kOffK + b * C::kBlockBytes, &tmK, b * 64, bhk, k_tok + k0, bar(B_KV));
+                    tma_load_3d(sb + C::kOffV + b * C::kBlockBytes, &tmV, b * 64, bhk, k_tok + k0, bar(B_KV));
+                } else {
+                    tma_load_3d(sb + C::kOffK + b * C::kBlockBytes, &tmK, b * 64, k0, bhk, bar(B_KV));
+                    tma_load_3d(sb + C::kOffV + b * C::kBlockBytes, &tmV, b * 64, k0, bhk, bar(B_KV));
+                }
             }
             bool ok = true;
             StepCursor cur = cursor0;
@@ -255,12 +287,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int s = t % S_;
                 const uint32_t it = (uint32_t)(t / S_);
                 const int q0 = cur.q0, bh = cur.bh;
-                const size_t vec_row = (size_t)bh * Nq_pad;
+                const size_t vec_row = (size_t)bh * ld_rows + seq_off;
+                // Q and dO rows: (row, head) for dense tensors, (head, token) for packed ones
+                const int qy = VARLEN ? bh : q0, qz = VARLEN ? q_tok + q0 : bh;
                 ok = mbar_wait_backoff(bar(B_QEMPTY(s)), (it & 1u) ^ 1u, abort_flag, status, 32);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(B_QFULL(s)), C::kTileBytes + C::kVecBytes);
                 for (int b = 0; b < C::kBlocks; ++b)
-                    tma_load_3d(sb + C::kOffQ + s * C::kTileBytes + b * C::kBlockBytes, &tmQ, b * 64, q0, bh,
+                    tma_load_3d(sb + C::kOffQ + s * C::kTileBytes + b * C::kBlockBytes, &tmQ, b * 64, qy, qz,
                                 bar(B_QFULL(s)));
                 const uint32_t vdst = sb + C::kOffVec + s * C::kVecBytes;
                 bulk_load(vdst, args.lse2 + vec_row + q0, 512, bar(B_QFULL(s)));
@@ -271,7 +305,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(B_DOFULL(s)), C::kTileBytes);
                 for (int b = 0; b < C::kBlocks; ++b)
-                    tma_load_3d(sb + C::kOffDO + s * C::kTileBytes + b * C::kBlockBytes, &tmDO, b * 64, q0, bh,
+                    tma_load_3d(sb + C::kOffDO + s * C::kTileBytes + b * C::kBlockBytes, &tmDO, b * 64, qy, qz,
                                 bar(B_DOFULL(s)));
                 pend_do |= 1u << s;
                 par_do = (par_do & ~(1u << s)) | ((it & 1u) << s);
@@ -412,7 +446,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_DQFREE));
-                float *dst = args.dq_acc + ((size_t)bh * Nq_pad + q0) * 128 + qw * 32 + lane;
+                float *dst = args.dq_acc + ((size_t)bh * ld_rows + seq_off + q0) * 128 + qw * 32 + lane;
                 const int rows = Nq - q0;
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
@@ -428,7 +462,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (lane == 0) mbar_arrive(bar(B_DQFREE));
                 const int q = q0 + qw * 32 + lane;
                 if (q < Nq) {
-                    float4 *dst = reinterpret_cast<float4 *>(args.dq_acc + ((size_t)bh * Nq_pad + q) * 64);
+                    float4 *dst = reinterpret_cast<float4 *>(args.dq_acc + ((size_t)bh * ld_rows + seq_off + q) * 64);
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         atomicAdd(dst + e, make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
@@ -530,7 +564,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // Epilogue: this warp's half of the head dimension of dV_j and dK_j = scale * acc.
             // The tensor-memory loads are warp-collective: every lane takes part, and
             // only lanes whose key exists store.
-            const size_t orow = ((size_t)bhk * Nk + j) * D;
+            const size_t orow = VARLEN ? ((size_t)(k_tok + j) * H_kv + bhk) * D : ((size_t)bhk * Nk + j) * D;
 #pragma unroll 1
             for (int which = 0; which < 2; ++which) {
                 typename PK::T *dst_row = reinterpret_cast<typename PK::T *>(which == 0 ? args.dv : args.dk) + orow;
@@ -571,22 +605,68 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 }
 
+// Largest s in [0, n] with a[s] <= x, for a non-decreasing a with a[0] <= x: the
+// sequence that holds token (or workspace row) x, skipping empty sequences.
+__device__ __forceinline__ int seq_of(const int *a, int n, int x) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Variable-length batches: row_off[s] = sum over s' < s of ceil(len_q(s') / 128) * 128,
+// the first workspace row of sequence s (s = 0 .. num_seqs).  One warp.
+__global__ void fa_bwd_plan_kernel(const BwdArgs a) {
+    const int lane = threadIdx.x;
+    int base = 0;
+    if (lane == 0) a.row_off[0] = 0;
+    for (int s0 = 0; s0 < a.num_seqs; s0 += 32) {
+        const int s = s0 + lane;
+        int v = s < a.num_seqs ? (a.cu_q[s + 1] - a.cu_q[s] + kBwdBr - 1) / kBwdBr * kBwdBr : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
+        }
+        if (s < a.num_seqs) a.row_off[s + 1] = base + v;
+        base += __shfl_sync(0xffffffffu, v, 31);
+    }
+}
+
 // -D_i = -dO_i . O_i (fp32), -lse2_i = -LSE_i log2(e) (-inf where LSE_i = -inf and
-// on the padding rows Nq <= i < Nq_pad, so that P = 2^(x - lse2) = 0 there), and the
-// row of the dQ accumulator zeroed.  One warp per row of [BH][Nq_pad].
-template <int D, bool BF16>
+// on the padding rows, so that P = 2^(x - lse2) = 0 there), and the row of the dQ
+// accumulator zeroed.  One warp per workspace row: [BH][Nq_pad] (dense; rows
+// q >= Nq are padding) or [H][rows_pad] (VARLEN; row row_off[s] + r holds token
+// cu_q[s] + r when r < len_q(s), every other row is padding).
+template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdArgs a) {
     using PK = Pack<BF16>;
     const int lane = threadIdx.x & 31;
-    const long long rows = (long long)a.BH * a.Nq_pad;
+    const int ld = VARLEN ? a.rows_pad : a.Nq_pad;
+    const long long rows = (long long)a.BH * ld;
     const long long stride = (long long)gridDim.x * 8;
     for (long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); row < rows; row += stride) {
-        const int bh = (int)(row / a.Nq_pad), q = (int)(row % a.Nq_pad);
+        const int bh = (int)(row / ld), q = (int)(row % ld);
         float4 *acc = reinterpret_cast<float4 *>(a.dq_acc + row * D);
         if (lane < D / 4) acc[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+        bool real;
+        size_t off, lse_idx;
+        if constexpr (VARLEN) {
+            const int s = seq_of(a.row_off, a.num_seqs, q);
+            const int r = q - a.row_off[s];
+            real = s < a.num_seqs && r < a.cu_q[s + 1] - a.cu_q[s];
+            const int tok = real ? a.cu_q[s] + r : 0;
+            off = ((size_t)tok * a.BH + bh) * D;         // [total_q, H, d]
+            lse_idx = (size_t)bh * a.total_q + tok;     // [H, total_q]
+        } else {
+            real = q < a.Nq;
+            off = ((size_t)bh * a.Nq + q) * D;
+            lse_idx = (size_t)bh * a.Nq + q;
+        }
         float dot = 0.f, l2 = INFINITY;
-        if (q < a.Nq) {
-            const size_t off = ((size_t)bh * a.Nq + q) * D;
+        if (real) {
             const uint32_t *o32 = reinterpret_cast<const uint32_t *>(static_cast<const typename PK::T *>(a.o) + off);
             const uint32_t *g32 = reinterpret_cast<const uint32_t *>(static_cast<const typename PK::T *>(a.dout) + off);
 #pragma unroll
@@ -597,7 +677,7 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdArgs a) {
             }
 #pragma unroll
             for (int sft = 16; sft > 0; sft >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, sft);
-            const float lse = a.lse[(size_t)bh * a.Nq + q];
+            const float lse = a.lse[lse_idx];
             l2 = (lse == -INFINITY) ? INFINITY : lse * 1.4426950408889634f;
         }
         if (lane == 0) {  // stored negated: the main kernel adds them
@@ -608,15 +688,25 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdArgs a) {
 }
 
 // dQ = scale * accumulator, rounded to 16 bits; four elements per thread step.
-template <int D, bool BF16>
+// Output rows: [BH][Nq] (dense) or [total_q][H] (VARLEN).
+template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a) {
     using PK = Pack<BF16>;
-    const long long n4 = (long long)a.BH * a.Nq * (D / 4);
+    const long long nrows = VARLEN ? (long long)a.total_q * a.BH : (long long)a.BH * a.Nq;
+    const long long n4 = nrows * (D / 4);
     for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n4; x += (long long)gridDim.x * blockDim.x) {
         const long long row = x / (D / 4);
         const int c4 = (int)(x % (D / 4));
-        const int bh = (int)(row / a.Nq), q = (int)(row % a.Nq);
-        const float4 v = reinterpret_cast<const float4 *>(a.dq_acc + ((size_t)bh * a.Nq_pad + q) * D)[c4];
+        size_t acc_row;
+        if constexpr (VARLEN) {
+            const int tok = (int)(row / a.BH), h = (int)(row % a.BH);
+            const int s = seq_of(a.cu_q, a.num_seqs, tok);
+            acc_row = (size_t)h * a.rows_pad + a.row_off[s] + (tok - a.cu_q[s]);
+        } else {
+            const int bh = (int)(row / a.Nq), q = (int)(row % a.Nq);
+            acc_row = (size_t)bh * a.Nq_pad + q;
+        }
+        const float4 v = reinterpret_cast<const float4 *>(a.dq_acc + acc_row * D)[c4];
         uint2 out;
         out.x = PK::pack(v.x * a.scale, v.y * a.scale);
         out.y = PK::pack(v.z * a.scale, v.w * a.scale);
@@ -624,31 +714,46 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a) {
     }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool VARLEN>
 static cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                                const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream) {
+                                const CUtensorMap &tdo, const BwdArgs &a, int max_seqlen_k, cudaStream_t stream) {
     using C = BwdCfg<D>;
-    const long long rows = (long long)a.BH * a.Nq_pad;
+    cudaError_t e;
+    if constexpr (VARLEN) {
+        e = launch_kernel(fa_bwd_plan_kernel, dim3(1), dim3(32), 0, stream, a);
+        if (e != cudaSuccess) return e;
+    }
+    const long long rows = (long long)a.BH * (VARLEN ? a.rows_pad : a.Nq_pad);
     const unsigned prep_blocks = (unsigned)std::min<long long>((rows + 7) / 8, 152LL * 64);
-    cudaError_t e = launch_kernel(fa_bwd_prep_kernel<D, BF16>, dim3(prep_blocks), dim3(256), 0, stream, a);
+    e = launch_kernel(fa_bwd_prep_kernel<D, BF16, VARLEN>, dim3(prep_blocks), dim3(256), 0, stream, a);
     if (e != cudaSuccess) return e;
-    auto kern = fa_bwd_kernel<D, BF16>;
+    auto kern = fa_bwd_kernel<D, BF16, VARLEN>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)((a.Nk + kBwdBc - 1) / kBwdBc), (unsigned)(a.BH / a.group), 1);
+    const int H_kv = a.H / a.group;
+    const dim3 grid = VARLEN ? dim3((unsigned)((max_seqlen_k + kBwdBc - 1) / kBwdBc), (unsigned)(a.num_seqs * H_kv), 1)
+                             : dim3((unsigned)((a.Nk + kBwdBc - 1) / kBwdBc), (unsigned)(a.BH / a.group), 1);
     e = launch_kernel(kern, grid, dim3(kBwdThreads), C::kSmemBytes, stream, tq, tk, tv, tdo, a);
     if (e != cudaSuccess) return e;
-    const long long n4 = (long long)a.BH * a.Nq * (D / 4);
-    const unsigned dq_blocks = (unsigned)std::min<long long>((n4 + 255) / 256, 152LL * 64);
-    return launch_kernel(fa_bwd_dq_kernel<D, BF16>, dim3(dq_blocks), dim3(256), 0, stream, a);
+    const long long n4 = (VARLEN ? (long long)a.total_q * a.BH : (long long)a.BH * a.Nq) * (D / 4);
+    const unsigned dq_blocks = (unsigned)std::min<long long>(std::max<long long>((n4 + 255) / 256, 1), 152LL * 64);
+    return launch_kernel(fa_bwd_dq_kernel<D, BF16, VARLEN>, dim3(dq_blocks), dim3(256), 0, stream, a);
 }
 
 cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream) {
-    if (d == 64) return bf16 ? launch_bwd_t<64, true>(tq, tk, tv, tdo, a, stream)
-                             : launch_bwd_t<64, false>(tq, tk, tv, tdo, a, stream);
-    return bf16 ? launch_bwd_t<128, true>(tq, tk, tv, tdo, a, stream)
-                : launch_bwd_t<128, false>(tq, tk, tv, tdo, a, stream);
+    if (d == 64) return bf16 ? launch_bwd_t<64, true, false>(tq, tk, tv, tdo, a, 0, stream)
+                             : launch_bwd_t<64, false, false>(tq, tk, tv, tdo, a, 0, stream);
+    return bf16 ? launch_bwd_t<128, true, false>(tq, tk, tv, tdo, a, 0, stream)
+                : launch_bwd_t<128, false, false>(tq, tk, tv, tdo, a, 0, stream);
+}
+
+cudaError_t launch_bwd_varlen(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                              const CUtensorMap &tdo, const BwdArgs &a, int max_seqlen_k, cudaStream_t stream) {
+    if (d == 64) return bf16 ? launch_bwd_t<64, true, true>(tq, tk, tv, tdo, a, max_seqlen_k, stream)
+                             : launch_bwd_t<64, false, true>(tq, tk, tv, tdo, a, max_seqlen_k, stream);
+    return bf16 ? launch_bwd_t<128, true, true>(tq, tk, tv, tdo, a, max_seqlen_k, stream)
+                : launch_bwd_t<128, false, true>(tq, tk, tv, tdo, a, max_seqlen_k, stream);
 }
 
 }  // namespace fa

@@ -79,6 +79,13 @@ struct BwdArgs {
     int causal;
     float scale;       // softmax scale
     float scale_log2;  // scale * log2(e)
+    // Variable-length batches (packed [total, heads, d] tensors; lse [H, total_q]):
+    // token offsets per sequence, and row_off[s], the first row of sequence s in the
+    // workspace's per-head row space, where every sequence starts on a multiple of
+    // 128 rows (written by the plan kernel); rows_pad rows per head.  Null for dense.
+    const int *cu_q, *cu_k;
+    int *row_off;
+    int num_seqs, total_q, rows_pad;
 };
 
 // FP8 (E4M3) forward: blocks of 128 rows of one head carry one fp32 scale each.
@@ -119,5 +126,9 @@ cudaError_t launch_selftest_timeout(int *status, int limit_ms, cudaStream_t stre
 // Backward: preprocess (D, lse2, zero dq_acc), the main K/V-block kernel, dQ conversion.
 cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream);
+// Variable-length form: packed tensor maps (column, head, token), grid
+// (ceil(max_seqlen_k / 128), num_seqs * H_kv); a.cu_q, a.cu_k, a.row_off set.
+cudaError_t launch_bwd_varlen(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                              const CUtensorMap &tdo, const BwdArgs &a, int max_seqlen_k, cudaStream_t stream);
 
 }  // namespace fa

@@ -121,10 +121,11 @@ def compare_grads(got, ref, mags, floors, dtype: torch.dtype, what: str = ""):
         err = np.abs(gg - r)
         tol = u * (m + np.abs(r)) + fl
         stats[name + "_max_err"] = float(err.max(initial=0.0))
-        stats[name + "_max_err_over_tol"] = float((err / tol).max(initial=0.0))
+        ratio = np.where(tol > 0, err / np.where(tol > 0, tol, 1.0), np.where(err > 0, np.inf, 0.0))
+        stats[name + "_max_err_over_tol"] = float(ratio.max(initial=0.0))
         bad = err > tol
         if bad.any():
-            idx = np.unravel_index(np.argmax(err / tol), err.shape)
+            idx = np.unravel_index(np.argmax(ratio), err.shape)
             raise AssertionError(f"{what}: {int(bad.sum())} {name} elements out of tolerance; worst at {idx}: "
                                  f"gpu={gg[idx]!r} ref={r[idx]!r} tol={tol[idx]!r}")
     return stats

@@ -126,3 +126,25 @@ def test_backward_and_fp8_validation_without_gpu(lib):
     assert f(p, None, p, p, p, p, p, None, 1, 2, 8, 8, 128, 0, 0.1, 1, None) == -1   # null q_scale
     assert f(p, p, p, p, odd, p, p, None, 1, 2, 8, 8, 128, 0, 0.1, 1, None) == -3    # v8t misaligned
     assert lib.fa_selftest_timeout(0, None) == -1
+    vb = lib.fa_bwd_varlen
+    two = ctypes.c_void_p((1 << 20) + 2)
+    args = lambda **o: [o.get(n, x) for n, x in (
+        ("q", p), ("k", p), ("v", p), ("o", p), ("dout", p), ("lse", p), ("dq", p), ("dk", p), ("dv", p),
+        ("cu_q", p), ("cu_k", p), ("num_seqs", 2), ("max_k", 20), ("total_q", 30), ("total_k", 30), ("H", 2),
+        ("H_kv", 2), ("d", 64), ("causal", 1), ("scale", 0.1), ("dtype", 1), ("ws", p), ("bytes", ws),
+        ("stream", None))]
+    assert vb(*args(dout=None)) == -1
+    assert vb(*args(lse=None)) == -1
+    assert vb(*args(cu_k=None)) == -1
+    assert vb(*args(max_k=0)) == -1
+    assert vb(*args(max_k=31)) == -1
+    assert vb(*args(num_seqs=0)) == -1
+    assert vb(*args(H=6, H_kv=4)) == -1
+    assert vb(*args(d=96)) == -2
+    assert vb(*args(dq=odd)) == -3
+    assert vb(*args(cu_q=two)) == -3
+    assert vb(*args(ws=None)) == -4
+    need = lib.fa_bwd_varlen_workspace_bytes(2, 30, 2, 64)
+    # offsets, then per head 128 (ceil(30 / 128) + 2) rows of 64 floats and two vectors
+    assert need == 256 + 2 * 384 * 64 * 4 + 2 * (2 * 384 * 4)
+    assert vb(*args(bytes=need - 1)) == -4

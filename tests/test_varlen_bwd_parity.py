@@ -1,0 +1,158 @@
+"""fa_bwd_varlen (backward of packed variable-length batches) against the fp64 oracle.
+
+Layouts as fa_fwd_varlen: q, o, dout, dq packed [total_q, H, d]; k, v, dk, dv
+[total_k, H_kv, d]; lse [H, total_q].  The GPU side runs fa_fwd_varlen then
+fa_bwd_varlen; the oracle recomputes each sequence's gradients from q, k, v, dO
+(oracle.attention_bwd_varlen).  Tolerance as in parity.compare_grads, with the
+magnitudes taken sequence by sequence.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attn_inputs
+import oracle
+from parity import compare_grads, grad_magnitudes
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import exact_attention_forward_03_gb300 as fa
+    from exact_attention_forward_03_gb300 import build
+
+    build.build()
+    fa.load_library()
+    oracle.set_threads(16)
+    return fa
+
+
+def _np(t):
+    return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def _packed(lens_q, lens_k, H, H_kv, d, dtype, seed):
+    total_q, total_k = sum(lens_q), sum(lens_k)
+    q, _, _ = attn_inputs.make_qkv(1, total_q, H, 1, d, dtype, seed, "cuda")
+    _, k, v = attn_inputs.make_qkv(1, total_k, 1, H_kv, d, dtype, seed + 5, "cuda")
+    dout = attn_inputs.make_dout(1, total_q, H, d, dtype, seed, "cuda")
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(lens_q)]), dtype=torch.int32, device="cuda")
+    cu_k = torch.tensor(np.concatenate([[0], np.cumsum(lens_k)]), dtype=torch.int32, device="cuda")
+    return q[0].contiguous(), k[0].contiguous(), v[0].contiguous(), dout[0].contiguous(), cu_q, cu_k
+
+
+def _magnitudes(q, k, v, dout, o_ref, lse_ref, lens_q, lens_k, causal, scale):
+    """grad_magnitudes sequence by sequence (K/V heads repeated per group, their
+    magnitudes summed like the gradients), in the packed layouts."""
+    H, H_kv, d = q.shape[1], k.shape[1], q.shape[2]
+    group = H // H_kv
+    mq, mk, mv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+    cq, ck = np.concatenate([[0], np.cumsum(lens_q)]), np.concatenate([[0], np.cumsum(lens_k)])
+    tr = lambda x: np.ascontiguousarray(x.transpose(1, 0, 2))           # [n, h, d] -> [h, n, d]
+    rep = lambda x: tr(x).repeat(group, axis=0)
+    for s in range(len(lens_q)):
+        a, b, c, e = cq[s], cq[s + 1], ck[s], ck[s + 1]
+        if b == a or e == c:
+            continue
+        m = grad_magnitudes(tr(q[a:b]), rep(k[c:e]), rep(v[c:e]), tr(o_ref[a:b]), tr(dout[a:b]),
+                            lse_ref[:, a:b], causal, scale)
+        mq[a:b] = m[0].transpose(1, 0, 2)
+        mk[c:e] = m[1].reshape(H_kv, group, e - c, d).sum(axis=1).transpose(1, 0, 2)
+        mv[c:e] = m[2].reshape(H_kv, group, e - c, d).sum(axis=1).transpose(1, 0, 2)
+    return mq, mk, mv
+
+
+def run_varlen_bwd(fa, lens_q, lens_k, H, H_kv, d, dtype, causal, seed):
+    q, k, v, dout, cu_q, cu_k = _packed(lens_q, lens_k, H, H_kv, d, dtype, seed)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa.fwd_varlen(q, k, v, cu_q, cu_k, max(lens_q), causal=causal, scale=scale)
+    dq, dk, dv = fa.bwd_varlen(q, k, v, o, dout, lse, cu_q, cu_k, max(lens_k), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.get_device_status() == fa.FA_OK
+    qn, kn, vn, gn = (_np(x) for x in (q, k, v, dout))
+    ref = oracle.attention_bwd_varlen(qn, kn, vn, gn, cu_q.cpu(), cu_k.cpu(), causal, scale)
+    o_ref, lse_ref = oracle.attention_varlen(qn, kn, vn, cu_q.cpu(), cu_k.cpu(), causal, scale)
+    mags = _magnitudes(qn, kn, vn, gn, o_ref, lse_ref, lens_q, lens_k, causal, scale)
+    floors = (0.0, 0.0, 0.0)
+    if q.dtype == torch.float16:  # fp32 accumulation of up to max-length sums, as in the dense test
+        e = 2.0 ** -25
+        group = H // H_kv
+        floors = (e * max(lens_k) * scale * np.abs(kn).max(), e * max(lens_q) * group * scale * np.abs(qn).max(),
+                  e * max(lens_q) * group * np.abs(gn).max())
+    compare_grads((dq, dk, dv), ref, mags, floors, q.dtype, f"bwd varlen q{lens_q} k{lens_k} H{H}/{H_kv} d{d}")
+    return dq, dk, dv, ref
+
+
+CASES = [
+    # lens_q, lens_k, H, H_kv, d, dtype, causal
+    ([1, 127, 128, 129, 300], None, 4, 4, 128, "bf16", True),
+    ([1, 127, 128, 129, 300], None, 4, 2, 64, "f16", False),
+    ([513, 7, 256], [600, 7, 100], 2, 1, 128, "bf16", True),     # Nq != Nk per sequence, some rows see no key
+    ([64, 0, 200], [64, 50, 0], 4, 2, 128, "bf16", False),        # an empty sequence and a keyless one
+    ([130, 0, 70], [0, 90, 70], 2, 2, 64, "bf16", True),          # keys without queries and queries without keys
+    ([1000, 1, 333, 1100], None, 8, 2, 128, "bf16", True),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"q{'-'.join(map(str, c[0]))}_H{c[2]}kv{c[3]}_d{c[4]}{c[5]}{'c' if c[6] else ''}")
+def test_bwd_varlen(fa, case):
+    lens_q, lens_k, H, H_kv, d, dtype, causal = case
+    lens_k = lens_k or lens_q
+    dq, dk, dv, ref = run_varlen_bwd(fa, lens_q, lens_k, H, H_kv, d, dtype, causal, 300 + sum(lens_q) % 97)
+    # sequences without keys: dQ exactly 0; keys of sequences without queries: dK = dV = 0
+    cq, ck = np.concatenate([[0], np.cumsum(lens_q)]), np.concatenate([[0], np.cumsum(lens_k)])
+    for s in range(len(lens_q)):
+        if lens_k[s] == 0 and lens_q[s] > 0:
+            assert (dq[cq[s]:cq[s + 1]] == 0).all()
+        if lens_q[s] == 0 and lens_k[s] > 0:
+            assert (dk[ck[s]:ck[s + 1]] == 0).all() and (dv[ck[s]:ck[s + 1]] == 0).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_equal_lengths_match_the_dense_backward(fa, causal):
+    """Packed sequences of one length are a dense batch.  Rows and keys past a
+    sequence end get weight exactly 0, so dK and dV (no atomics) agree with fa_bwd
+    to the bit; dQ (fp32 atomic sums, order not fixed) within a few ulp."""
+    B, H, N, d = 3, 4, 300, 128
+    q, k, v = attn_inputs.make_qkv(B, H, N, N, d, "bf16", 211, "cuda")
+    dout = attn_inputs.make_dout(B, H, N, d, "bf16", 211, "cuda")
+    o, lse = fa.fwd(q, k, v, causal=causal)
+    dq_d, dk_d, dv_d = fa.bwd(q, k, v, o, dout, lse, causal=causal)
+    pack = lambda x: x.transpose(1, 2).reshape(B * N, H, d).contiguous()
+    cu = torch.arange(0, (B + 1) * N, N, dtype=torch.int32, device="cuda")
+    lse_p = lse.transpose(0, 1).reshape(H, B * N).contiguous()
+    dq, dk, dv = fa.bwd_varlen(pack(q), pack(k), pack(v), pack(o), pack(dout), lse_p, cu, cu, N, causal=causal)
+    torch.cuda.synchronize()
+    assert fa.get_device_status() == fa.FA_OK
+    assert torch.equal(dk, pack(dk_d))
+    assert torch.equal(dv, pack(dv_d))
+    diff = (dq.float() - pack(dq_d).float()).abs()
+    assert (diff <= 2.0 ** -6 * pack(dq_d).float().abs() + 1e-6).all()
+
+
+def test_varlen_bwd_deterministic_dk_dv(fa):
+    q, k, v, dout, cu_q, cu_k = _packed([300, 5, 700], [300, 5, 700], 4, 2, 128, "bf16", 77)
+    o, lse = fa.fwd_varlen(q, k, v, cu_q, cu_k, 700, causal=True)
+    a = fa.bwd_varlen(q, k, v, o, dout, lse, cu_q, cu_k, 700, causal=True)
+    b = fa.bwd_varlen(q, k, v, o, dout, lse, cu_q, cu_k, 700, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+def test_varlen_bwd_rejects_bad_arguments(fa):
+    q, k, v, dout, cu_q, cu_k = _packed([10, 20], [10, 20], 2, 2, 64, "bf16", 5)
+    o, lse = fa.fwd_varlen(q, k, v, cu_q, cu_k, 20)
+    with pytest.raises(fa.FaError) as e:
+        fa.bwd_varlen(q, k, v, o, dout, lse, cu_q, cu_k, 0)    # max_seqlen_k must be >= 1
+    assert e.value.code == fa.FA_ERR_INVALID_ARG
+    with pytest.raises(fa.FaError) as e:
+        fa.bwd_varlen(q, k, v, o, dout, lse, cu_q, cu_k, 31)   # more than total_k
+    assert e.value.code == fa.FA_ERR_INVALID_ARG
+    short = torch.empty(fa.bwd_varlen_workspace_bytes(2, 30, 2, 64) - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.FaError) as e:
+        fa.bwd_varlen(q, k, v, o, dout, lse, cu_q, cu_k, 20, workspace=short)
+    assert e.value.code == fa.FA_ERR_WORKSPACE
+    assert fa.get_device_status() == fa.FA_OK
