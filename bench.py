@@ -360,7 +360,7 @@ def run_fa(args, rank, world, local):
                                         f"combine) excluded: {part_bytes} bytes per call")}}
 
     # ---- packed variable-length batch (fa_fwd_varlen)
-    varlen = None
+    varlen = varlen_bwd = None
     if not args.no_varlen:
         vw = attn_inputs.VARLEN_WORKLOAD
         lens = attn_inputs.varlen_lengths(vw["num_seqs"], vw["lo"], vw["hi"], vw["seed"])
@@ -386,6 +386,34 @@ def run_fa(args, rank, world, local):
                   "roofline": {"bound": "tensor", "achieved": vflops / (vmean * 1e-3) / 1e12,
                                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                "frac": vflops / (vmean * 1e-3) / 1e12 / peaks["bf16_tflops"], "traffic": None}}
+        if not args.no_bwd:
+            # the backward of the same packed batch (fa_bwd_varlen: plan, preprocess, main kernel, dQ conversion)
+            vg = attn_inputs.make_dout(1, total, vw["H"], vw["d"], vw["dtype"], vw["seed"], dev)[0]
+            vdq, vdk, vdv = torch.empty_like(vq), torch.empty_like(vk), torch.empty_like(vv)
+            vws = torch.empty(fa.bwd_varlen_workspace_bytes(len(lens), total, vw["H"], vw["d"]), dtype=torch.uint8,
+                              device=dev)
+            vcall()
+
+            def vbcall():
+                fa.bwd_varlen(vq, vk, vv, vo, vg, vl, cu, cu, max(lens), causal=vw["causal"], dq=vdq, dk=vdk, dv=vdv,
+                              workspace=vws)
+
+            vbms = time_calls(vbcall, args.steps, args.warmup, flush)
+            launches += 4 * args.steps
+            vbmean = statistics.mean(vbms)
+            vbflops = 2.5 * vflops
+            varlen_bwd = {"workload": vw["name"], "entry_point": "fa_bwd_varlen", "launches_per_call": 4,
+                          "ms_per_call": vbmean,
+                          "value": sum_over_ranks(vbflops, world) / (max_over_ranks(vbmean, world) * 1e-3) / 1e12,
+                          "unit": "TFLOP/s", "flops_per_call": vbflops,
+                          "roofline": {"bound": "tensor", "achieved": vbflops / (vbmean * 1e-3) / 1e12,
+                                       "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                       "frac": vbflops / (vbmean * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                                       "traffic": None,
+                                       "note": "whole call (four launches) timed; FLOPs 2.5x the forward's"}}
+            if fa.get_device_status() != fa.FA_OK:
+                raise RuntimeError("device status not ok after the variable-length backward")
+            del vg, vdq, vdk, vdv, vws
         del vq, vk, vv, vo, vl
         torch.cuda.empty_cache()
 
@@ -509,7 +537,7 @@ def run_fa(args, rank, world, local):
                      "peak_source": peak_src,
                      "kernel": "fa_fwd_kernel<128,bf16>", "flops_per_launch": flops},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "decode": decode,
-        "decode_gqa": decode_gqa, "varlen": varlen, "bwd": bwd, "fp8": fp8,
+        "decode_gqa": decode_gqa, "varlen": varlen, "varlen_bwd": varlen_bwd, "bwd": bwd, "fp8": fp8,
         "wall_s_fwd_timed": wall, "ms_fwd_min": min(ms), "ms_fwd_median": statistics.median(ms),
     }
     if rank == 0:

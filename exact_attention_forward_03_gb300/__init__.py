@@ -406,6 +406,32 @@ def bwd_varlen(q, k, v, o, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_k: 
     return dq, dk, dv
 
 
+class _AttentionVarlen(torch.autograd.Function):
+    """Forward through fa_fwd_varlen, backward through fa_bwd_varlen."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, cu_q, cu_k, max_q, max_k, causal, scale):
+        o, lse = fwd_varlen(q, k, v, cu_q, cu_k, max_q, causal=causal, scale=scale)
+        ctx.save_for_backward(q, k, v, o, lse, cu_q, cu_k)
+        ctx.max_k, ctx.causal, ctx.scale = max_k, causal, scale
+        return o
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, o, lse, cu_q, cu_k = ctx.saved_tensors
+        dq, dk, dv = bwd_varlen(q, k, v, o, dout.contiguous(), lse, cu_q, cu_k, ctx.max_k, causal=ctx.causal,
+                                scale=ctx.scale)
+        return dq, dk, dv, None, None, None, None, None, None
+
+
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                     causal: bool = False, scale: float | None = None):
+    """Differentiable attention of a packed variable-length batch: fa_fwd_varlen in
+    the forward pass, fa_bwd_varlen in the backward (layouts as ``fwd_varlen``)."""
+    return _AttentionVarlen.apply(q, k, v, cu_seqlens_q, cu_seqlens_k, int(max_seqlen_q), int(max_seqlen_k), causal,
+                                  scale)
+
+
 def splitkv_num_splits(B, H, Nq, Nk, d) -> int:
     return load_library().fa_splitkv_num_splits(B, H, Nq, Nk, d)
 

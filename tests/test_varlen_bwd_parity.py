@@ -156,3 +156,17 @@ def test_varlen_bwd_rejects_bad_arguments(fa):
         fa.bwd_varlen(q, k, v, o, dout, lse, cu_q, cu_k, 20, workspace=short)
     assert e.value.code == fa.FA_ERR_WORKSPACE
     assert fa.get_device_status() == fa.FA_OK
+
+
+def test_varlen_autograd(fa):
+    """attention_varlen under autograd gives the gradients of fa_bwd_varlen."""
+    q, k, v, dout, cu_q, cu_k = _packed([90, 200, 31], [120, 200, 40], 4, 2, 64, "bf16", 91)
+    qq, kk, vv = (x.clone().requires_grad_(True) for x in (q, k, v))
+    out = fa.attention_varlen(qq, kk, vv, cu_q, cu_k, 200, 200, causal=True)
+    out.backward(dout)
+    o, lse = fa.fwd_varlen(q, k, v, cu_q, cu_k, 200, causal=True)
+    dq, dk, dv = fa.bwd_varlen(q, k, v, o, dout, lse, cu_q, cu_k, 200, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out.detach(), o)
+    assert torch.equal(kk.grad, dk) and torch.equal(vv.grad, dv)
+    assert ((qq.grad.float() - dq.float()).abs() <= 2.0 ** -6 * dq.float().abs() + 1e-6).all()
