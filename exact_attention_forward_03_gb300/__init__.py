@@ -45,7 +45,8 @@ EXPORTS = ("fa_fwd", "fa_fwd_splitkv", "fa_splitkv_combine", "fa_splitkv_workspa
            "fa_splitkv_num_splits", "fa_splitkv_split_len", "fa_get_device_status", "fa_status_string",
            "fa_version", "fa_fwd_splitkv_noalloc", "fa_splitkv_noalloc_capacity_bytes", "fa_fwd_gqa",
            "fa_fwd_splitkv_gqa", "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace_bytes", "fa_last_error", "fa_fp8_quantize", "fa_fwd_fp8", "fa_selftest_timeout", "fa_bwd_gqa",
-           "fa_bwd_varlen", "fa_bwd_varlen_workspace_bytes")
+           "fa_bwd_varlen", "fa_bwd_varlen_workspace_bytes", "fa_fwd_host",
+           "fa_fwd_host_workspace_bytes")
 
 _lock = threading.Lock()
 _lib = None
@@ -111,6 +112,10 @@ def load_library(path: str | None = None):
         lib.fa_bwd_varlen.restype = i
         lib.fa_bwd_varlen_workspace_bytes.argtypes = [i, i, i, i]
         lib.fa_bwd_varlen_workspace_bytes.restype = sz
+        lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, vp, sz, vp]
+        lib.fa_fwd_host.restype = i
+        lib.fa_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        lib.fa_fwd_host_workspace_bytes.restype = sz
         lib.fa_fp8_quantize.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
         lib.fa_fp8_quantize.restype = i
         lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
@@ -196,6 +201,51 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
                             int(bool(causal)), scale, _dtype_code(q), _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd" if H_kv == H else "fa_fwd_gqa")
+    return out, lse
+
+
+def fwd_host_workspace_bytes(B, H, H_kv, Nq, Nk, d) -> int:
+    return int(load_library().fa_fwd_host_workspace_bytes(B, H, H_kv, Nq, Nk, d))
+
+
+def fwd_host(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, want_lse: bool = True,
+             num_chunks: int = 0, workspace=None, stream=None, synchronize: bool = True):
+    """Forward from and to host memory through ``fa_fwd_host``: q [B, H, Nq, d], k, v
+    [B, H_kv, Nk, d] CPU tensors (page-locked for overlapped copies); returns (o, lse)
+    as CPU tensors (page-locked when allocated here).  The copies and the kernels are
+    queued on ``stream`` (the current stream by default); with ``synchronize`` the
+    call waits for that stream before returning."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU [B, H, N, d] tensor")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    B, H, Nq, d = q.shape
+    H_kv, Nk = k.shape[1], k.shape[2]
+    if k.shape[0] != B or v.shape != k.shape or k.shape[3] != d or H_kv <= 0 or H % H_kv != 0:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    elif out.is_cuda or out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CPU tensor like q")
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, pin_memory=True)
+    elif lse is not None and (lse.is_cuda or lse.shape != (B, H, Nq) or lse.dtype != torch.float32
+                              or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 CPU [B, H, Nq] tensor")
+    lib = load_library()
+    need = fwd_host_workspace_bytes(B, H, H_kv, Nq, Nk, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+    rc = lib.fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         lse.data_ptr() if lse is not None else None, B, H, H_kv, Nq, Nk, d, int(bool(causal)), scale,
+                         _dtype_code(q), int(num_chunks), workspace.data_ptr(),
+                         workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_host")
+    if synchronize:
+        (stream if stream is not None else torch.cuda.current_stream()).synchronize()
     return out, lse
 
 

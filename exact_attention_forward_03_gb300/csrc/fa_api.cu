@@ -33,6 +33,13 @@ struct DeviceState {
     bool ready = false;
     int *status = nullptr;  // device address of g_status_word
     int num_sms = 0;
+    // fa_fwd_host: copy-in and copy-out streams and the events that order them
+    // against the caller's stream, created on first use; host_mu serialises the
+    // enqueueing of calls that share them.
+    bool host_ready = false;
+    cudaStream_t copy_in = nullptr, copy_out = nullptr;
+    cudaEvent_t ev_entry = nullptr, ev_in = nullptr, ev_comp = nullptr, ev_exit = nullptr;
+    std::mutex host_mu;
 };
 
 std::mutex g_mu;
@@ -228,6 +235,85 @@ int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
     a.scale_log2 = scale * 1.4426950408889634f;
     cudaError_t e = launch_fwd(d, bf16, tq, tk, tv, a, BH, reinterpret_cast<cudaStream_t>(stream));
     return launch_status("kernel launch", e);
+}
+
+size_t fa_fwd_host_workspace_bytes(int B, int H, int H_kv, int Nq, int Nk, int d) {
+    if (B <= 0 || H <= 0 || H_kv <= 0 || H % H_kv != 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return 0;
+    const size_t qb = (size_t)B * H * Nq * d * 2, kb = (size_t)B * H_kv * Nk * d * 2;
+    return 2 * align256(qb) + 2 * align256(kb) + align256((size_t)B * H * Nq * sizeof(float));
+}
+
+int fa_fwd_host(const void *q_host, const void *k_host, const void *v_host, void *o_host, float *lse_host, int B,
+                int H, int H_kv, int Nq, int Nk, int d, int causal, float scale, fa_dtype dtype, int num_chunks,
+                void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+    if (q_host == nullptr || k_host == nullptr || v_host == nullptr || o_host == nullptr) return FA_ERR_INVALID_ARG;
+    // The checks of fa_fwd_gqa on stand-in device pointers (the workspace's are only known below).
+    const void *probe = reinterpret_cast<const void *>((uintptr_t)256);
+    int rc = check_common(probe, probe, probe, probe, nullptr, B, H, Nq, Nk, d, causal, scale, dtype);
+    if (rc != FA_OK) return rc;
+    if (H_kv <= 0 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
+    const size_t need = fa_fwd_host_workspace_bytes(B, H, H_kv, Nq, Nk, d);
+    if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    DeviceState *st = nullptr;
+    if ((rc = dev_state(&st)) != FA_OK) return rc;
+    std::lock_guard<std::mutex> lk(st->host_mu);
+    cudaError_t e;
+    if (!st->host_ready) {
+        if ((e = cudaStreamCreateWithFlags(&st->copy_in, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&st->copy_out, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&st->ev_entry, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&st->ev_in, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&st->ev_comp, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&st->ev_exit, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail("fa_fwd_host stream setup", e);
+        st->host_ready = true;
+    }
+    const int group = H / H_kv;
+    const int kv_heads = B * H_kv;
+    int chunks = num_chunks > 0 ? num_chunks : 8;
+    if (chunks > kv_heads) chunks = kv_heads;
+    const size_t q_head = (size_t)Nq * d * 2, k_head = (size_t)Nk * d * 2;  // bytes per head
+    char *ws = static_cast<char *>(workspace);
+    char *qd = ws;
+    char *od = qd + align256((size_t)B * H * q_head);
+    char *kd = od + align256((size_t)B * H * q_head);
+    char *vd = kd + align256((size_t)kv_heads * k_head);
+    float *ld = reinterpret_cast<float *>(vd + align256((size_t)kv_heads * k_head));
+    const char *qh = static_cast<const char *>(q_host), *kh = static_cast<const char *>(k_host),
+               *vh = static_cast<const char *>(v_host);
+    char *oh = static_cast<char *>(o_host);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const auto h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+    if ((e = cudaEventRecord(st->ev_entry, cs)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(st->copy_in, st->ev_entry, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(st->copy_out, st->ev_entry, 0)) != cudaSuccess)
+        return cuda_fail("fa_fwd_host ordering", e);
+    for (int c = 0; c < chunks; ++c) {
+        // K/V heads [h0, h1) and their query heads [h0 * group, h1 * group)
+        const int h0 = (int)((long long)kv_heads * c / chunks), h1 = (int)((long long)kv_heads * (c + 1) / chunks);
+        const size_t qo = (size_t)h0 * group * q_head, qn = (size_t)(h1 - h0) * group * q_head;
+        const size_t ko = (size_t)h0 * k_head, kn = (size_t)(h1 - h0) * k_head;
+        const size_t lo = (size_t)h0 * group * Nq, ln = (size_t)(h1 - h0) * group * Nq;  // lse elements
+        if ((e = cudaMemcpyAsync(qd + qo, qh + qo, qn, h2d, st->copy_in)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(kd + ko, kh + ko, kn, h2d, st->copy_in)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(vd + ko, vh + ko, kn, h2d, st->copy_in)) != cudaSuccess ||
+            (e = cudaEventRecord(st->ev_in, st->copy_in)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(cs, st->ev_in, 0)) != cudaSuccess)
+            return cuda_fail("fa_fwd_host copy in", e);
+        rc = fa_fwd_gqa(qd + qo, kd + ko, vd + ko, od + qo, ld + lo, 1, (h1 - h0) * group, h1 - h0, Nq, Nk, d, causal,
+                        scale, dtype, stream);
+        if (rc != FA_OK) return rc;
+        if ((e = cudaEventRecord(st->ev_comp, cs)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(st->copy_out, st->ev_comp, 0)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(oh + qo, od + qo, qn, d2h, st->copy_out)) != cudaSuccess ||
+            (lse_host != nullptr &&
+             (e = cudaMemcpyAsync(lse_host + lo, ld + lo, ln * sizeof(float), d2h, st->copy_out)) != cudaSuccess))
+            return cuda_fail("fa_fwd_host copy out", e);
+    }
+    if ((e = cudaEventRecord(st->ev_exit, st->copy_out)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(cs, st->ev_exit, 0)) != cudaSuccess)
+        return cuda_fail("fa_fwd_host ordering", e);
+    return FA_OK;
 }
 
 int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, const int *cu_seqlens_q,

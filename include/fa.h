@@ -233,6 +233,37 @@ FA_API int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, v
 FA_API size_t fa_splitkv_noalloc_capacity_bytes(void);
 
 /*
+ * Forward from and to HOST memory, with the copies overlapped with the compute.
+ * q_host, k_host, v_host, o_host, lse_host hold what fa_fwd_gqa's q, k, v, o, lse
+ * hold, in the same layouts, in host memory (lse_host may be NULL).  The K/V
+ * heads (B * H_kv of them, with their H / H_kv query heads each) are cut into
+ * num_chunks consecutive chunks (num_chunks <= 0: min(B * H_kv, 8)); chunk c's
+ * inputs are copied to the device on a copy stream while chunk c - 1 is computed
+ * on `stream` and chunk c - 2's output is copied back on a second copy stream.
+ * Each chunk runs the fa_fwd_gqa kernels on its heads, so o and lse equal
+ * fa_fwd_gqa's bit for bit.  The call is ordered on `stream` like a kernel
+ * launch: the copies start after the work queued on `stream` before the call,
+ * and o_host, lse_host hold the result once `stream` has reached the point of the
+ * call's return (synchronize `stream` before reading them).  Host buffers should
+ * be page-locked (cudaHostAlloc / cudaHostRegister); with pageable memory the
+ * results are the same but the copies do not overlap.
+ * Workspace: device memory of at least fa_fwd_host_workspace_bytes(B, H, H_kv,
+ * Nq, Nk, d) bytes, 256-byte aligned, owned by the caller (the device copies of
+ * q, k, v, o and lse); free for reuse once `stream` has passed the call.  The
+ * two copy streams and their events belong to the library (one set per device;
+ * concurrent calls on one device share them, which orders their copies).
+ * Errors: as fa_fwd_gqa; FA_ERR_INVALID_ARG for a null host pointer (lse_host
+ * excepted); FA_ERR_WORKSPACE for a null, misaligned or short workspace;
+ * FA_ERR_CUDA if a copy or stream operation fails (outputs then unspecified).
+ * (The pages time the kernel with its inputs resident; this entry point is the
+ * end-to-end form of the same "Flash Attention (4)" §5 forward.)
+ */
+FA_API size_t fa_fwd_host_workspace_bytes(int B, int H, int H_kv, int Nq, int Nk, int d);
+FA_API int fa_fwd_host(const void *q_host, const void *k_host, const void *v_host, void *o_host, float *lse_host,
+                       int B, int H, int H_kv, int Nq, int Nk, int d, int causal, float scale, fa_dtype dtype,
+                       int num_chunks, void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * Attention backward: the gradients dQ, dK, dV of O = softmax(scale * Q K^T +
  * mask) V given dO, for the same mask as the forward ("Lecture 25" §3.3, the
  * backward with P recomputed from the saved statistics; "02 · FA2:

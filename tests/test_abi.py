@@ -148,3 +148,11 @@ def test_backward_and_fp8_validation_without_gpu(lib):
     # offsets, then per head 128 (ceil(30 / 128) + 2) rows of 64 floats and two vectors
     assert need == 256 + 2 * 384 * 64 * 4 + 2 * (2 * 384 * 4)
     assert vb(*args(bytes=need - 1)) == -4
+    h = lib.fa_fwd_host
+    assert h(None, p, p, p, p, 1, 2, 2, 8, 8, 64, 0, 0.1, 1, 0, p, ws, None) == -1       # null q_host
+    assert h(p, p, p, p, p, 1, 6, 4, 8, 8, 64, 0, 0.1, 1, 0, p, ws, None) == -1          # 6 % 4 != 0
+    assert h(p, p, p, p, p, 1, 2, 2, 8, 8, 96, 0, 0.1, 1, 0, p, ws, None) == -2          # d = 96
+    assert h(p, p, p, p, p, 1, 2, 2, 8, 8, 64, 0, 0.1, 1, 0, None, ws, None) == -4       # no workspace
+    hneed = lib.fa_fwd_host_workspace_bytes(1, 2, 2, 8, 8, 64)
+    assert hneed == 4 * 2048 + 256                        # q, o, k, v (2 heads x 8 x 64 x 2 B), lse
+    assert h(p, p, p, p, p, 1, 2, 2, 8, 8, 64, 0, 0.1, 1, 0, p, hneed - 1, None) == -4  # short workspace
