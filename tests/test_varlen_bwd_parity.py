@@ -94,10 +94,17 @@ CASES = [
     ([64, 0, 200], [64, 50, 0], 4, 2, 128, "bf16", False),        # an empty sequence and a keyless one
     ([130, 0, 70], [0, 90, 70], 2, 2, 64, "bf16", True),          # keys without queries and queries without keys
     ([1000, 1, 333, 1100], None, 8, 2, 128, "bf16", True),
+    # 100 short sequences (several 32-sequence chunks of the row plan), lengths 0..300, some empty
+    ([int(x) for x in np.random.default_rng(5).integers(0, 301, 100)], None, 2, 1, 64, "bf16", True),
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: f"q{'-'.join(map(str, c[0]))}_H{c[2]}kv{c[3]}_d{c[4]}{c[5]}{'c' if c[6] else ''}")
+def _case_id(c):
+    lens = "-".join(map(str, c[0])) if len(c[0]) <= 6 else f"{len(c[0])}seqs"
+    return f"q{lens}_H{c[2]}kv{c[3]}_d{c[4]}{c[5]}{'c' if c[6] else ''}"
+
+
+@pytest.mark.parametrize("case", CASES, ids=_case_id)
 def test_bwd_varlen(fa, case):
     lens_q, lens_k, H, H_kv, d, dtype, causal = case
     lens_k = lens_k or lens_q
@@ -170,3 +177,44 @@ def test_varlen_autograd(fa):
     assert torch.equal(out.detach(), o)
     assert torch.equal(kk.grad, dk) and torch.equal(vv.grad, dv)
     assert ((qq.grad.float() - dq.float()).abs() <= 2.0 ** -6 * dq.float().abs() + 1e-6).all()
+
+
+def _segment_sums(x, cu):
+    """Per-sequence sums over tokens of a [total, H, d] tensor (fp64): [num_seqs, H, d]."""
+    c = torch.cat([torch.zeros_like(x[:1], dtype=torch.float64), x.double().cumsum(dim=0)])
+    return c[cu[1:].long()] - c[cu[:-1].long()]
+
+
+def test_bwd_varlen_benchmarked_batch(fa):
+    """The benchmarked packed batch (16 causal sequences of 256..8192 tokens, H=32,
+    d=128, bf16): on every sequence and head the dK rows sum to zero and the dV rows
+    to the dO rows, and one head of the longest sequence against the oracle."""
+    import itertools
+
+    vw = attn_inputs.VARLEN_WORKLOAD
+    lens = attn_inputs.varlen_lengths(vw["num_seqs"], vw["lo"], vw["hi"], vw["seed"])
+    total, H, d = sum(lens), vw["H"], vw["d"]
+    q = attn_inputs.make_qkv(1, total, H, 1, d, vw["dtype"], vw["seed"], "cuda")[0][0]
+    _, k, v = attn_inputs.make_qkv(1, total, 1, H, d, vw["dtype"], vw["seed"] + 5, "cuda")
+    k, v = k[0], v[0]
+    dout = attn_inputs.make_dout(1, total, H, d, vw["dtype"], vw["seed"], "cuda")[0]
+    cu = torch.tensor([0] + list(itertools.accumulate(lens)), dtype=torch.int32, device="cuda")
+    o, lse = fa.fwd_varlen(q, k, v, cu, cu, max(lens), causal=True)
+    dq, dk, dv = fa.bwd_varlen(q, k, v, o, dout, lse, cu, cu, max(lens), causal=True)
+    torch.cuda.synchronize()
+    assert fa.get_device_status() == fa.FA_OK
+    assert torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
+    u = 2.0 ** -8
+    s_dk = _segment_sums(dk, cu).abs()
+    assert (s_dk <= 2 * u * _segment_sums(dk.abs(), cu) + 1e-6).all()
+    s_dv, s_do = _segment_sums(dv, cu), _segment_sums(dout, cu)
+    assert ((s_dv - s_do).abs() <= 2 * u * (_segment_sums(dv.abs(), cu) + _segment_sums(dout.abs(), cu))).all()
+    s = int(np.argmax(lens))
+    a, b, h = int(cu[s]), int(cu[s + 1]), 11
+    one = lambda x: _np(x[a:b, h]).reshape(1, b - a, d)
+    scale = 1.0 / math.sqrt(d)
+    ref = oracle.attention_bwd(one(q), one(k), one(v), one(dout), True, scale)
+    o_ref, lse_ref = oracle.attention(one(q), one(k), one(v), True, scale)
+    mags = grad_magnitudes(one(q), one(k), one(v), o_ref, one(dout), lse_ref, True, scale)
+    compare_grads((dq[a:b, h], dk[a:b, h], dv[a:b, h]), ref, mags, (0.0, 0.0, 0.0), torch.bfloat16,
+                  f"bwd varlen benchmarked batch, sequence {s} ({lens[s]} tokens), head {h}")

@@ -44,10 +44,17 @@ CASES = [
     ([513, 7, 256], [600, 7, 100], 2, 1, 128, "bf16", True),     # Nq != Nk per sequence, some rows see no key
     ([64, 0, 200], [64, 50, 0], 4, 2, 128, "bf16", False),        # an empty sequence and a keyless one
     ([1000, 1, 333, 2048], None, 8, 2, 128, "bf16", True),
+    # 100 short sequences, lengths 0..300 (two of them empty)
+    ([int(x) for x in np.random.default_rng(5).integers(0, 301, 100)], None, 2, 1, 64, "bf16", True),
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: f"q{'-'.join(map(str, c[0]))}_H{c[2]}kv{c[3]}_d{c[4]}{c[5]}{'c' if c[6] else ''}")
+def _case_id(c):
+    lens = "-".join(map(str, c[0])) if len(c[0]) <= 6 else f"{len(c[0])}seqs"
+    return f"q{lens}_H{c[2]}kv{c[3]}_d{c[4]}{c[5]}{'c' if c[6] else ''}"
+
+
+@pytest.mark.parametrize("case", CASES, ids=_case_id)
 def test_varlen(fa, case):
     lens_q, lens_k, H, H_kv, d, dtype, causal = case
     lens_k = lens_k or lens_q
