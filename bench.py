@@ -466,11 +466,17 @@ def run_fa(args, rank, world, local):
         qms = time_calls(qcall, max(3, min(args.steps, 20)), args.warmup, flush)
         launches += args.steps + 3 * max(3, min(args.steps, 20))
         fmean = statistics.mean(fms)
+        qbytes = 3.0 * q.numel() * (q.element_size() + 1) + 3.0 * w.B * w.H * ((w.Nq + 127) // 128) * 4
         fpeak = 2.0 * peaks["bf16_tflops"]  # E4M3 dense rate = 2x bf16 (nominal 4.5 vs 2.25 PFLOP/s)
         fach = flops / (fmean * 1e-3) / 1e12
         fp8 = {"workload": w.name, "entry_point": "fa_fwd_fp8", "ms_per_call": fmean, "ms_min": min(fms),
                "value": sum_over_ranks(flops, world) / (max_over_ranks(fmean, world) * 1e-3) / 1e12, "unit": "TFLOP/s",
                "quantize_ms_per_call": statistics.mean(qms),
+               "quantize_roofline": {"bound": "hbm", "unit": "GB/s", "peak": peaks["hbm_gbs"],
+                                     "achieved": qbytes / (statistics.mean(qms) * 1e-3) / 1e9,
+                                     "frac": qbytes / (statistics.mean(qms) * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                     "note": "fa_fp8_quantize of Q, K, V: 16-bit inputs read, E4M3 codes and "
+                                             "per-block scales written (compulsory bytes)"},
                "roofline": {"bound": "tensor", "achieved": fach, "peak": fpeak, "unit": "TFLOP/s", "frac": fach / fpeak,
                             "traffic": captured_traffic("fa_fwd_fp8_kernel<bf16>", w.name),
                             "note": "inputs quantized beforehand (fa_fp8_quantize of Q, K, V timed separately as "

@@ -92,35 +92,69 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float v0, float v1, float v2, fl
 }
 
 // ----------------------------------------------------------------------------- quantization
-// One CTA per block of 128 rows of one head (blockIdx.x = block, blockIdx.y = head);
-// thread t holds row t / 2, columns 64 (t % 2) ... + 63.
+// x / s rounded to the nearest fp32, given y = 1/s rounded to the nearest fp32:
+// two residual corrections with exact FMA residuals.  q0 = x y is within 1.5 ulp
+// of x / s, q1 = q0 + (x - s q0) y within one ulp, and by Markstein's theorem
+// (P. Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Develop. 34(1), 1990) q1 + (x - s q1) y rounded is the
+// rounded quotient, provided nothing overflows or underflows on the way.  The
+// quantizer divides every element of a block by the block's one s, so the
+// reciprocal is taken once per block and each element costs one multiply and four
+// FMAs.  The sign is taken from x (s > 0): the corrections would turn x = -0 into
+// +0, and a quotient that underflows to zero keeps its sign.
+__device__ __forceinline__ float div_rn_by(float x, float s, float y) {
+    const float q0 = __fmul_rn(x, y);
+    const float r0 = __fmaf_rn(-q0, s, x);
+    const float q1 = __fmaf_rn(r0, y, q0);
+    const float r1 = __fmaf_rn(-q1, s, x);
+    return copysignf(__fmaf_rn(r1, y, q1), x);
+}
+
+// One CTA per block of 128 rows of one head (blockIdx.x = block, blockIdx.y = head).
+// Global memory is only touched with lane-consecutive 16-byte accesses: the
+// block's 32 KB come in as 2048 consecutive chunks, go to shared memory with row
+// r's chunk j at r * 256 + 16 (j ^ (r mod 16)) (the XOR keeps both the writes and
+// the per-row reads below free of bank conflicts), thread t then takes row t / 2,
+// columns 64 (t mod 2) ... + 63, and the codes leave through the same buffer:
+// row-major with the 16-byte chunk k of row r at r * 128 + 16 (k ^ (r mod 8)), or
+// for V transposed, [column][row], one 128-byte output row per head-dim index.
 template <bool BF16, bool TRANSPOSE>
-__global__ void __launch_bounds__(256) fa_fp8_quant_kernel(const Fp8QuantArgs a) {
+__global__ void __launch_bounds__(256, 3) fa_fp8_quant_kernel(const Fp8QuantArgs a) {
     using PK = Pack<BF16>;
     __shared__ float warp_max[8];
-    __shared__ __align__(16) uint8_t tile[TRANSPOSE ? 128 * 128 : 16];
-    const int t = threadIdx.x, r = t >> 1, half = t & 1;
+    __shared__ __align__(16) uint8_t xs[128 * 256];
+    const int t = threadIdx.x;
     const int blk = blockIdx.x, bh = blockIdx.y;
-    const int row = blk * 128 + r;
-    const bool valid = row < a.N;
-    float x[64];
-    if (valid) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const typename PK::T *>(a.x) +
-                                                           ((size_t)bh * a.N + row) * 128 + 64 * half);
+    const int rows = min(128, a.N - blk * 128);  // rows of this block inside the tensor
+    const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(a.x) +
+                                                       ((size_t)bh * a.N + (size_t)blk * 128) * 256);
+    {
+        uint4 v[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const uint4 u = src[e];
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 f = PK::unpack(w[k]);
-                x[8 * e + 2 * k] = f.x;
-                x[8 * e + 2 * k + 1] = f.y;
-            }
+            const int id = t + 256 * e;  // chunk id: row id / 16, chunk id % 16
+            v[e] = (id >> 4) < rows ? src[id] : make_uint4(0u, 0u, 0u, 0u);
         }
-    } else {
 #pragma unroll
-        for (int e = 0; e < 64; ++e) x[e] = 0.f;
+        for (int e = 0; e < 8; ++e) {
+            const int id = t + 256 * e, row = id >> 4, j = id & 15;
+            *reinterpret_cast<uint4 *>(xs + row * 256 + ((j ^ (row & 15)) << 4)) = v[e];
+        }
+    }
+    __syncthreads();
+    const int r = t >> 1, half = t & 1;
+    float x[64];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const int j = half * 8 + e;
+        const uint4 u = *reinterpret_cast<const uint4 *>(xs + r * 256 + ((j ^ (r & 15)) << 4));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = PK::unpack(w[k]);
+            x[8 * e + 2 * k] = f.x;
+            x[8 * e + 2 * k + 1] = f.y;
+        }
     }
     float amax = 0.f;
 #pragma unroll
@@ -128,35 +162,56 @@ __global__ void __launch_bounds__(256) fa_fp8_quant_kernel(const Fp8QuantArgs a)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     if ((t & 31) == 0) warp_max[t >> 5] = amax;
-    __syncthreads();
+    __syncthreads();  // also: every thread has read its inputs out of xs
     amax = warp_max[0];
 #pragma unroll
     for (int w = 1; w < 8; ++w) amax = fmaxf(amax, warp_max[w]);
     const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
     if (t == 0) a.scales[(size_t)bh * a.num_blocks + blk] = s;
     uint32_t c[16];
+    if (s >= 0x1p-60f && s <= 0x1p100f) {
+        // With 2^-60 <= s <= 2^100, 1/s and every product stay finite, and for each x
+        // whose quotient can round to a nonzero code (|x / s| >= 2^-10) the residuals
+        // (about 2^-24 |x| >= 2^-94) stay normal; smaller quotients give a signed
+        // zero code whatever their last bits.
+        const float y = __frcp_rn(s);
 #pragma unroll
-    for (int e = 0; e < 16; ++e)
-        c[e] = pack_e4m3x4(__fdiv_rn(x[4 * e], s), __fdiv_rn(x[4 * e + 1], s), __fdiv_rn(x[4 * e + 2], s),
-                           __fdiv_rn(x[4 * e + 3], s));
+        for (int e = 0; e < 16; ++e)
+            c[e] = pack_e4m3x4(div_rn_by(x[4 * e], s, y), div_rn_by(x[4 * e + 1], s, y),
+                               div_rn_by(x[4 * e + 2], s, y), div_rn_by(x[4 * e + 3], s, y));
+    } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            c[e] = pack_e4m3x4(__fdiv_rn(x[4 * e], s), __fdiv_rn(x[4 * e + 1], s), __fdiv_rn(x[4 * e + 2], s),
+                               __fdiv_rn(x[4 * e + 3], s));
+    }
     if constexpr (!TRANSPOSE) {
-        if (valid) {
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(a.x8) + ((size_t)bh * a.N + row) * 128 +
-                                                   64 * half);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(c[4 * e], c[4 * e + 1], c[4 * e + 2], c[4 * e + 3]);
+        for (int e = 0; e < 4; ++e) {
+            const int k = 4 * half + e;  // 16-byte chunk of the 128-byte code row
+            *reinterpret_cast<uint4 *>(xs + r * 128 + ((k ^ (r & 7)) << 4)) =
+                make_uint4(c[4 * e], c[4 * e + 1], c[4 * e + 2], c[4 * e + 3]);
+        }
+        __syncthreads();
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(a.x8) + ((size_t)bh * a.N + (size_t)blk * 128) * 128);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int id = t + 256 * e, row = id >> 3, k = id & 7;
+            if (row < rows) dst[id] = *reinterpret_cast<const uint4 *>(xs + row * 128 + ((k ^ (row & 7)) << 4));
         }
     } else {
-        // tile[col][row]: column (head-dim index) major, then one 128-byte row of
-        // codes per head-dim index goes out to [BH, d, N_pad].  Rows past N hold 0.
+        // [column][row]: rows past N carry x = 0, so code 0 (the padding the
+        // transposed layout asks for)
 #pragma unroll
-        for (int e = 0; e < 64; ++e) tile[(64 * half + e) * 128 + r] = (uint8_t)(c[e >> 2] >> (8 * (e & 3)));
+        for (int e = 0; e < 64; ++e) xs[(64 * half + e) * 128 + r] = (uint8_t)(c[e >> 2] >> (8 * (e & 3)));
         __syncthreads();
-        const uint4 *srow = reinterpret_cast<const uint4 *>(tile + r * 128 + 64 * half);
-        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(a.x8) + ((size_t)bh * 128 + r) * a.ld_t +
-                                               (size_t)blk * 128 + 64 * half);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) dst[e] = srow[e];
+        for (int e = 0; e < 4; ++e) {
+            const int id = t + 256 * e, col = id >> 3, k = id & 7;
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(a.x8) + ((size_t)bh * 128 + col) * a.ld_t +
+                                                   (size_t)blk * 128 + 16 * k);
+            *dst = *reinterpret_cast<const uint4 *>(xs + col * 128 + 16 * k);
+        }
     }
 }
 
