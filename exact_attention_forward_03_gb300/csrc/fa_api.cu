@@ -284,10 +284,20 @@ int fa_fwd_host(const void *q_host, const void *k_host, const void *v_host, void
     char *oh = static_cast<char *>(o_host);
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const auto h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+    // On an error after copies were queued, `stream` is still made to wait for them,
+    // so that a caller who synchronises it may free the buffers.
+    auto join = [&]() {
+        if (cudaEventRecord(st->ev_in, st->copy_in) == cudaSuccess) cudaStreamWaitEvent(cs, st->ev_in, 0);
+        if (cudaEventRecord(st->ev_exit, st->copy_out) == cudaSuccess) cudaStreamWaitEvent(cs, st->ev_exit, 0);
+    };
+    auto join_and_fail = [&](const char *what, cudaError_t err) {
+        join();
+        return cuda_fail(what, err);
+    };
     if ((e = cudaEventRecord(st->ev_entry, cs)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(st->copy_in, st->ev_entry, 0)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(st->copy_out, st->ev_entry, 0)) != cudaSuccess)
-        return cuda_fail("fa_fwd_host ordering", e);
+        return join_and_fail("fa_fwd_host ordering", e);
     for (int c = 0; c < chunks; ++c) {
         // K/V heads [h0, h1) and their query heads [h0 * group, h1 * group)
         const int h0 = (int)((long long)kv_heads * c / chunks), h1 = (int)((long long)kv_heads * (c + 1) / chunks);
@@ -299,20 +309,23 @@ int fa_fwd_host(const void *q_host, const void *k_host, const void *v_host, void
             (e = cudaMemcpyAsync(vd + ko, vh + ko, kn, h2d, st->copy_in)) != cudaSuccess ||
             (e = cudaEventRecord(st->ev_in, st->copy_in)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(cs, st->ev_in, 0)) != cudaSuccess)
-            return cuda_fail("fa_fwd_host copy in", e);
+            return join_and_fail("fa_fwd_host copy in", e);
         rc = fa_fwd_gqa(qd + qo, kd + ko, vd + ko, od + qo, ld + lo, 1, (h1 - h0) * group, h1 - h0, Nq, Nk, d, causal,
                         scale, dtype, stream);
-        if (rc != FA_OK) return rc;
+        if (rc != FA_OK) {
+            join();
+            return rc;
+        }
         if ((e = cudaEventRecord(st->ev_comp, cs)) != cudaSuccess ||
             (e = cudaStreamWaitEvent(st->copy_out, st->ev_comp, 0)) != cudaSuccess ||
             (e = cudaMemcpyAsync(oh + qo, od + qo, qn, d2h, st->copy_out)) != cudaSuccess ||
             (lse_host != nullptr &&
              (e = cudaMemcpyAsync(lse_host + lo, ld + lo, ln * sizeof(float), d2h, st->copy_out)) != cudaSuccess))
-            return cuda_fail("fa_fwd_host copy out", e);
+            return join_and_fail("fa_fwd_host copy out", e);
     }
     if ((e = cudaEventRecord(st->ev_exit, st->copy_out)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(cs, st->ev_exit, 0)) != cudaSuccess)
-        return cuda_fail("fa_fwd_host ordering", e);
+        return join_and_fail("fa_fwd_host ordering", e);
     return FA_OK;
 }
 
