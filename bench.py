@@ -8,9 +8,13 @@ causal, timed with CUDA events around every fa_fwd launch on the launching
 stream, with the L2 cache flushed (a 256 MiB write) before each timed launch.
 The split-KV decode path (B=32, H=32, Nq=1, Nk=16384, d=128, bf16, 16 splits)
 is timed the same way and reported under "decode" in GB/s, and its grouped-query
-form (32 query heads over 8 K/V heads) under "decode_gqa".  The backward of the
-default workload (fa_bwd, 2.5x the forward's FLOPs) is reported under "bwd", and
-its FP8 (E4M3) forward from pre-quantized inputs under "fp8".
+form (32 query heads over 8 K/V heads) under "decode_gqa".  A packed batch of 16
+causal sequences of 256..8192 tokens goes under "varlen" (forward) and
+"varlen_bwd" (its backward).  The backward of the default workload (fa_bwd, 2.5x
+the forward's FLOPs) is reported under "bwd", and its FP8 (E4M3) forward from
+pre-quantized inputs under "fp8" (with the quantization of Q, K, V timed beside
+it).  "e2e" runs the default workload through fa_fwd_host: host buffers in and
+out, the copies inside the timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fa|reference]
 
