@@ -140,30 +140,33 @@ def sample_rows(Nq: int, BH: int, count: int, seed: int, tile: int = 128):
 
     Always present for bh = 0 and bh = BH - 1: rows 0, 1, tile-1, tile, tile+1,
     Nq-1, and the first and last row of a middle tile (clipped to [0, Nq)).
-    The rest are drawn uniformly without replacement.
+    The rest are drawn uniformly without replacement, in the order of one
+    seeded permutation of all BH * Nq pairs.  Linear in `count`: membership is
+    tested against a set.
     """
     g = torch.Generator().manual_seed(seed)
     mid = (Nq // tile // 2) * tile
     fixed_rows = [0, 1, tile - 1, tile, tile + 1, Nq - 1, mid, mid + tile - 1]
-    picks = []
+    out: list[tuple[int, int]] = []
+    seen: set[tuple[int, int]] = set()
+    n_fixed = 0
     for bh in sorted({0, BH - 1}):
         for r in fixed_rows:
             if 0 <= r < Nq:
-                picks.append((bh, r))
+                n_fixed += 1
+                if (bh, r) not in seen:
+                    seen.add((bh, r))
+                    out.append((bh, r))
     total = BH * Nq
-    want = max(0, min(count, total) - len(set(picks)))
-    if want > 0:
-        idx = torch.randperm(total, generator=g)[: want + len(picks)].tolist()
+    target = min(count, total)
+    if len(out) < target:
+        # every fixed pair can collide with at most one drawn pair, so this prefix always suffices
+        idx = torch.randperm(total, generator=g)[: target - len(out) + n_fixed].tolist()
         for flat in idx:
             p = (flat // Nq, flat % Nq)
-            if p not in picks:
-                picks.append(p)
-            if len(set(picks)) >= min(count, total):
-                break
-    seen = set()
-    out = []
-    for p in picks:
-        if p not in seen:
-            seen.add(p)
-            out.append(p)
+            if p not in seen:
+                seen.add(p)
+                out.append(p)
+                if len(out) >= target:
+                    break
     return out

@@ -339,3 +339,34 @@ def sampled_rows(q, k, v, pairs, causal: bool, scale: float, heads_per_batch: in
         o[idx] = oo
         lse[idx] = ll
     return o, lse
+
+
+class WidenedWorkload:
+    """A workload's Q, K and V widened to fp64 once, for repeated row queries.
+
+    ``sampled_rows`` widens the heads it touches on every call; a caller that
+    evaluates many row samples of one workload (a timing loop) widens once
+    here, gathers each sample's query rows with ``gather`` and then calls
+    ``rows``, whose only work is the oracle's own arithmetic (attention_rows:
+    the plain definition per row over the row's full key range).
+    q: [B, H, Nq, d]; k, v: [B, H_kv, Nk, d] (H_kv divides H).
+    """
+
+    def __init__(self, q, k, v):
+        self.Nq, self.d = int(q.shape[-2]), int(q.shape[-1])
+        self.H, self.H_kv = int(q.shape[1]), int(k.shape[1])
+        self.q = to_f64(q).reshape(-1, self.Nq, self.d)
+        self.k = to_f64(k).reshape(-1, int(k.shape[-2]), self.d)
+        self.v = to_f64(v).reshape(-1, int(v.shape[-2]), self.d)
+
+    def gather(self, pairs):
+        """(query rows [n, d], row indices [n], K/V head slots [n]) of the (bh, row) pairs."""
+        a = np.asarray(pairs, dtype=np.int64).reshape(-1, 2)
+        bh, rows = a[:, 0], a[:, 1]
+        slots = (bh // self.H) * self.H_kv + (bh % self.H) // (self.H // self.H_kv)  # kv_head_of, vectorised
+        return np.ascontiguousarray(self.q[bh, rows]), np.ascontiguousarray(rows), np.ascontiguousarray(slots)
+
+    def rows(self, gathered, causal: bool, scale: float):
+        """Oracle (O [n, d], LSE [n]) of gathered rows."""
+        q_rows, rows, slots = gathered
+        return attention_rows(q_rows, rows, slots, self.k, self.v, self.Nq, causal, scale)
