@@ -14,7 +14,13 @@ causal sequences of 256..8192 tokens goes under "varlen" (forward) and
 the forward's FLOPs) is reported under "bwd", and its FP8 (E4M3) forward from
 pre-quantized inputs under "fp8" (with the quantization of Q, K, V timed beside
 it).  "e2e" runs the default workload through fa_fwd_host: host buffers in and
-out, the copies inside the timed region.
+out, the copies inside the timed region.  The fused forward at the benchmark's
+other workloads is timed the same way and reported with its own roofline under
+"cfg1" / "cfg1_causal" (B=1, H=1, N=128, d=64, fp16: one CTA, a latency case),
+"cfg2" / "cfg2_causal" (B=4, H=16, N=1024, d=64, fp16), "cfg3_noncausal" (the
+default shape without the mask) and "cfg4" (B=1, H=32, N=32768, d=128, bf16,
+causal); the decode workload at 8 and 32 splits under "decode_s8" and
+"decode_s32".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fa|reference]
 
@@ -319,28 +325,29 @@ def run_fa(args, rank, world, local):
     launches = args.steps
 
     # ---- decode (split-KV + combine): multi-head, and grouped-query (several query heads per K/V head)
-    def measure_decode(wd, fused=False):
-        dq, dk, dv = attn_inputs.make_workload(wd, dev)
+    def measure_decode(wd, fused=False, splits=None, inputs=None):
+        splits = args.decode_splits if splits is None else splits
+        dq, dk, dv = inputs if inputs is not None else attn_inputs.make_workload(wd, dev)
         do = torch.empty_like(dq)
         dl = torch.empty((wd.B, wd.H, wd.Nq), dtype=torch.float32, device=dev)
-        ws = fa.splitkv_workspace(dq, dk, args.decode_splits)
+        ws = fa.splitkv_workspace(dq, dk, splits)
 
         def dcall():
             if fused:  # fa_fwd_gqa: a group's query heads as the rows of one tensor-core tile
                 fa.fwd(dq, dk, dv, causal=False, scale=wd.scale, out=do, lse=dl)
             else:
-                fa.fwd_splitkv(dq, dk, dv, causal=False, scale=wd.scale, num_splits=args.decode_splits,
+                fa.fwd_splitkv(dq, dk, dv, causal=False, scale=wd.scale, num_splits=splits,
                                workspace=ws, out=do, lse=dl)
 
         dms = time_calls(dcall, args.steps, args.warmup, flush)
         dmean = statistics.mean(dms)
         dbytes = wd.compulsory_bytes()
         gbs = dbytes / (dmean * 1e-3) / 1e9
-        part_bytes = 2 * args.decode_splits * wd.B * wd.H * wd.Nq * (wd.d + 1) * 4
+        part_bytes = 2 * splits * wd.B * wd.H * wd.Nq * (wd.d + 1) * 4
         del dq, dk, dv, ws
         torch.cuda.empty_cache()
         return {"workload": wd.name, "entry_point": "fa_fwd_gqa" if fused else "fa_fwd_splitkv",
-                "num_splits": None if fused else args.decode_splits, "ms_per_call": dmean,
+                "num_splits": None if fused else splits, "ms_per_call": dmean,
                 "value": sum_over_ranks(dbytes, world) / (max_over_ranks(dmean, world) * 1e-3) / 1e9,
                 "unit": "GB/s",
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -348,6 +355,45 @@ def run_fa(args, rank, world, local):
                              "note": f"compulsory bytes (Q, K, V read, O, LSE written) per call; peak {peak_src}"
                                      + ("" if fused else "; split-partial traffic (written and re-read by the "
                                         f"combine) excluded: {part_bytes} bytes per call")}}
+
+    # ---- the fused forward at every other workload of the benchmark (one fa_fwd launch per call)
+    def measure_fwd(wname):
+        wf = attn_inputs.WORKLOADS[wname]
+        fq, fk, fv = attn_inputs.make_workload(wf, dev)
+        fo = torch.empty_like(fq)
+        fl = torch.empty((wf.B, wf.H, wf.Nq), dtype=torch.float32, device=dev)
+
+        def fcall():
+            fa.fwd(fq, fk, fv, causal=wf.causal, scale=wf.scale, out=fo, lse=fl)
+
+        fms = time_calls(fcall, args.steps, args.warmup, flush)
+        fmean = statistics.mean(fms)
+        if fa.get_device_status() != fa.FA_OK:
+            raise RuntimeError(f"device status not ok after {wname}")
+        fflops = wf.flops()
+        ach = fflops / (fmean * 1e-3) / 1e12
+        kern = f"fa_fwd_kernel<{wf.d},{wf.dtype}>"
+        del fq, fk, fv, fo, fl
+        torch.cuda.empty_cache()
+        return {"workload": wf.name, "entry_point": "fa_fwd", "ms_per_call": fmean, "us_per_call": 1e3 * fmean,
+                "ms_min": min(fms), "value": sum_over_ranks(fflops, world) / (max_over_ranks(fmean, world) * 1e-3) / 1e12,
+                "unit": "TFLOP/s", "flops_per_call": fflops, "grid_ctas": wf.B * wf.H * ((wf.Nq + 127) // 128),
+                "roofline": {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                             "frac": ach / peaks["bf16_tflops"],
+                             "frac_of_sustained": ach / peaks["bf16_tflops_sustained"],
+                             "traffic": captured_traffic(kern, wf.name), "kernel": kern,
+                             "note": "fp16 and bf16 share the dense 16-bit tensor rate; peak "
+                                     f"{peak_src} bf16 burst"}}
+
+    configs = {}
+    if not args.no_configs:
+        for key, wname in (("cfg1", "tiny_d64_f16"), ("cfg1_causal", "tiny_d64_f16_causal"),
+                           ("cfg2", "b4h16_n1024_d64_f16"), ("cfg2_causal", "b4h16_n1024_d64_f16_causal"),
+                           ("cfg3_noncausal", "b2h32_n8192_d128_bf16"),
+                           ("cfg4", "b1h32_n32768_d128_bf16_causal")):
+            if wname != w.name:
+                configs[key] = measure_fwd(wname)
+                launches += args.steps
 
     # ---- packed variable-length batch (fa_fwd_varlen)
     varlen = varlen_bwd = None
@@ -478,8 +524,16 @@ def run_fa(args, rank, world, local):
     if not args.no_decode:
         del q, k, v
         torch.cuda.empty_cache()
-        decode = measure_decode(attn_inputs.WORKLOADS[args.decode_workload])
+        wdec = attn_inputs.WORKLOADS[args.decode_workload]
+        dec_in = attn_inputs.make_workload(wdec, dev)
+        decode = measure_decode(wdec, inputs=dec_in)
         launches += 2 * args.steps
+        for sp in (8, 32):  # the split count against the HBM roofline (16 is `decode`)
+            if sp != args.decode_splits:
+                configs[f"decode_s{sp}"] = measure_decode(wdec, splits=sp, inputs=dec_in)
+                launches += 2 * args.steps
+        del dec_in
+        torch.cuda.empty_cache()
         if args.decode_gqa_workload:
             decode_gqa = measure_decode(attn_inputs.WORKLOADS[args.decode_gqa_workload], fused=True)
             launches += args.steps
@@ -542,6 +596,7 @@ def run_fa(args, rank, world, local):
                      "kernel": "fa_fwd_kernel<128,bf16>", "flops_per_launch": flops},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "decode": decode,
         "decode_gqa": decode_gqa, "varlen": varlen, "varlen_bwd": varlen_bwd, "bwd": bwd, "fp8": fp8,
+        **configs,
         "wall_s_fwd_timed": wall, "ms_fwd_min": min(ms), "ms_fwd_median": statistics.median(ms),
     }
     if rank == 0:
@@ -580,6 +635,9 @@ def main(argv=None):
     ap.add_argument("--decode-gqa-workload", default="decode_b32h32kv8_nk16384_d128_bf16",
                     help="grouped-query decode workload reported under decode_gqa ('' to skip)")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the forward at the other workloads (cfg1, cfg1_causal, cfg2, cfg2_causal, "
+                         "cfg3_noncausal, cfg4)")
     ap.add_argument("--no-varlen", action="store_true")
     ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--no-fp8", action="store_true")
