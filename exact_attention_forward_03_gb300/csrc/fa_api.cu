@@ -215,9 +215,9 @@ int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
     if ((rc = dev_state(&st)) != FA_OK) return rc;
     const bool bf16 = dtype == FA_BF16;
     const int BH = B * H;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (make_map(&tq, q, bf16, d, Nq, BH, kFwdBr) != FA_OK || make_map(&tk, k, bf16, d, Nk, B * H_kv, kFwdBc) != FA_OK ||
-        make_map(&tv, v, bf16, d, Nk, B * H_kv, kFwdBc) != FA_OK)
+        make_map(&tv, v, bf16, d, Nk, B * H_kv, kFwdBc) != FA_OK || make_map(&to, o, bf16, d, Nq, BH, kFwdBr) != FA_OK)
         return FA_ERR_CUDA;
     FwdArgs a;
     a.o = o;
@@ -233,7 +233,7 @@ int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
     a.total_q = 0;
     a.causal = causal;
     a.scale_log2 = scale * 1.4426950408889634f;
-    cudaError_t e = launch_fwd(d, bf16, tq, tk, tv, a, BH, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_fwd(d, bf16, tq, tk, tv, to, a, BH, reinterpret_cast<cudaStream_t>(stream));
     return launch_status("kernel launch", e);
 }
 
@@ -343,10 +343,11 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *l
     DeviceState *st = nullptr;
     if ((rc = dev_state(&st)) != FA_OK) return rc;
     const bool bf16 = dtype == FA_BF16;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (make_map_packed(&tq, q, bf16, d, H, total_q, kFwdBr) != FA_OK ||
         make_map_packed(&tk, k, bf16, d, H_kv, total_k, kFwdBc) != FA_OK ||
-        make_map_packed(&tv, v, bf16, d, H_kv, total_k, kFwdBc) != FA_OK)
+        make_map_packed(&tv, v, bf16, d, H_kv, total_k, kFwdBc) != FA_OK ||
+        make_map_packed(&to, o, bf16, d, H, total_q, kFwdBr) != FA_OK)
         return FA_ERR_CUDA;
     FwdArgs a;
     a.o = o;
@@ -362,7 +363,7 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *l
     a.total_q = total_q;
     a.causal = causal;
     a.scale_log2 = scale * 1.4426950408889634f;
-    cudaError_t e = launch_fwd_varlen(d, bf16, tq, tk, tv, a, num_seqs, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_fwd_varlen(d, bf16, tq, tk, tv, to, a, num_seqs, reinterpret_cast<cudaStream_t>(stream));
     return launch_status("kernel launch", e);
 }
 

@@ -247,7 +247,8 @@ __device__ __noinline__ void rescale_o(uint32_t o_addr, float alpha) {
 template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const FwdArgs args) {
     using C = FwdCfg<D>;
     using PK = Pack<BF16>;
     extern __shared__ uint8_t smem_raw[];
@@ -325,6 +326,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmO);
     }
     if (warp == kWarpPv) {
         tmem_alloc(sb + C::kOffMisc, C::kTmemCols);
@@ -483,12 +485,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_OFINAL), 0, abort_flag, status));
             tc_fence_after();
         }
-        if (ok && __any_sync(0xffffffffu, i < Nq)) {
-            // Epilogue: O = O~ / l (0 for a row that saw no key), LSE = m ln2 + ln l.
-            const bool valid = i < Nq;
+        // Epilogue: O = O~ / l (0 for a row that saw no key), LSE = m ln2 + ln l.  The
+        // rows go through shared memory (K ring slot 0: every S MMA, hence every read
+        // of the K ring, completed before the last PV did) in the layout of a Q or K
+        // tile, and leave as TMA stores of whole 128-byte rows; rows past Nq are clipped
+        // by the tensor map.  A packed batch's last row block of a sequence stops short
+        // of the tile (its box would run into the next sequence's rows): its rows are
+        // stored directly.
+        const bool staged = !VARLEN || q0 + kFwdBr <= Nq;
+        const bool valid = i < Nq;
+        const int row = quarter * 32 + lane;
+        if (ok && __any_sync(0xffffffffu, valid)) {
             const float inv = (l > 0.f) ? 1.f / l : 0.f;
             const size_t orow = VARLEN ? (size_t)(q_tok + i) * args.H + bh % args.H : (size_t)bh * Nq + i;
             typename PK::T *orow_g = reinterpret_cast<typename PK::T *>(args.o) + orow * D;
+            uint8_t *stage_row = smem + C::kOffK + row * 128;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t ov[32];
@@ -503,7 +514,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     pk[e] = PK::pack(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
-                if (valid) {
+                if (staged) {
+                    // columns [32c, 32c+32): 64-column block c/2, 16-byte chunks 4(c%2)..4(c%2)+3,
+                    // chunk k of row r at r*128 + 16*(k ^ (r mod 8)) (the 128-byte swizzle)
+                    uint8_t *blk = stage_row + (c >> 1) * C::kKVBlockBytes;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int k = 4 * (c & 1) + e;
+                        *reinterpret_cast<uint4 *>(blk + 16 * (k ^ (row & 7))) =
+                            make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                    }
+                } else if (valid) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow_g + 32 * c);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
@@ -513,6 +534,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 const float m_fin = (m == -INFINITY) ? 0.f : m;
                 const size_t lrow = VARLEN ? (size_t)(bh % args.H) * args.total_q + q_tok + i : (size_t)bh * Nq + i;
                 args.lse[lrow] = (l > 0.f) ? m_fin * 0.69314718055994531f + logf(l) : -INFINITY;
+            }
+        }
+        if (staged) {
+            // Every softmax warp arrives (whatever its rows or its wait outcomes), so the
+            // barrier always completes; the stores go out only if no warp gave up a wait.
+            fence_proxy_async_smem();
+            const bool all_ok = named_bar_and(1, 128, ok);
+            if (all_ok && threadIdx.x == 0) {
+                for (int b = 0; b < C::kBlocks; ++b)
+                    if constexpr (VARLEN)
+                        tma_store_3d(&tmO, sb + C::kOffK + b * C::kKVBlockBytes, b * 64, bh % args.H, q_tok + q0);
+                    else
+                        tma_store_3d(&tmO, sb + C::kOffK + b * C::kKVBlockBytes, b * 64, q0, bh);
+                bulk_commit();
+                bulk_wait_read();
             }
         }
     }
@@ -528,32 +564,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
 template <int D, bool BF16, bool VARLEN>
 static cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                                const FwdArgs &a, int num_m, int rows_y, cudaStream_t stream) {
+                                const CUtensorMap &to, const FwdArgs &a, int num_m, int rows_y, cudaStream_t stream) {
     using C = FwdCfg<D>;
     auto kern = fa_fwd_kernel<D, BF16, VARLEN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)num_m, (unsigned)rows_y, 1);
-    return launch_kernel(kern, grid, dim3(kFwdThreads), C::kSmemBytes, stream, tq, tk, tv, a);
+    return launch_kernel(kern, grid, dim3(kFwdThreads), C::kSmemBytes, stream, tq, tk, tv, to, a);
 }
 
 template <bool VARLEN>
 static cudaError_t launch_fwd_any(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
-                                  const CUtensorMap &tv, const FwdArgs &a, int rows_y, cudaStream_t stream) {
-    if (d == 64) return bf16 ? launch_fwd_t<64, true, VARLEN>(tq, tk, tv, a, a.num_m, rows_y, stream)
-                             : launch_fwd_t<64, false, VARLEN>(tq, tk, tv, a, a.num_m, rows_y, stream);
-    return bf16 ? launch_fwd_t<128, true, VARLEN>(tq, tk, tv, a, a.num_m, rows_y, stream)
-                : launch_fwd_t<128, false, VARLEN>(tq, tk, tv, a, a.num_m, rows_y, stream);
+                                  const CUtensorMap &tv, const CUtensorMap &to, const FwdArgs &a, int rows_y,
+                                  cudaStream_t stream) {
+    if (d == 64) return bf16 ? launch_fwd_t<64, true, VARLEN>(tq, tk, tv, to, a, a.num_m, rows_y, stream)
+                             : launch_fwd_t<64, false, VARLEN>(tq, tk, tv, to, a, a.num_m, rows_y, stream);
+    return bf16 ? launch_fwd_t<128, true, VARLEN>(tq, tk, tv, to, a, a.num_m, rows_y, stream)
+                : launch_fwd_t<128, false, VARLEN>(tq, tk, tv, to, a, a.num_m, rows_y, stream);
 }
 
 cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const FwdArgs &a, int BH, cudaStream_t stream) {
-    return launch_fwd_any<false>(d, bf16, tq, tk, tv, a, BH, stream);
+                       const CUtensorMap &to, const FwdArgs &a, int BH, cudaStream_t stream) {
+    return launch_fwd_any<false>(d, bf16, tq, tk, tv, to, a, BH, stream);
 }
 
 cudaError_t launch_fwd_varlen(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                              const FwdArgs &a, int num_seqs, cudaStream_t stream) {
-    return launch_fwd_any<true>(d, bf16, tq, tk, tv, a, num_seqs * a.H, stream);
+                              const CUtensorMap &to, const FwdArgs &a, int num_seqs, cudaStream_t stream) {
+    return launch_fwd_any<true>(d, bf16, tq, tk, tv, to, a, num_seqs * a.H, stream);
 }
 
 }  // namespace fa

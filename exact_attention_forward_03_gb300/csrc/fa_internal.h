@@ -109,12 +109,14 @@ struct Fp8FwdArgs {
 };
 
 // Each launcher returns the CUDA error of the launch (cudaSuccess when queued).
+// The fused forward: `to` is O's tensor map (the same boxes as Q's), for the TMA
+// stores of the epilogue.
 cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const FwdArgs &a, int BH, cudaStream_t stream);
+                       const CUtensorMap &to, const FwdArgs &a, int BH, cudaStream_t stream);
 // Variable-length form: grid (num_m, num_seqs * H), packed tensor maps (x = column,
 // y = head, z = token), a.cu_q / a.cu_k set.
 cudaError_t launch_fwd_varlen(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                              const FwdArgs &a, int num_seqs, cudaStream_t stream);
+                              const CUtensorMap &to, const FwdArgs &a, int num_seqs, cudaStream_t stream);
 cudaError_t launch_splitkv(int d, bool bf16, const CUtensorMap &tk, const CUtensorMap &tv, const SplitArgs &a,
                            cudaStream_t stream);
 cudaError_t launch_combine(int d, bool bf16, const CombineArgs &a, cudaStream_t stream);
