@@ -408,15 +408,18 @@ def run_fa(args, rank, world, local):
         cu = torch.tensor([0] + list(itertools.accumulate(lens)), dtype=torch.int32, device=dev)
         vo = torch.empty_like(vq)
         vl = torch.empty((vw["H"], total), dtype=torch.float32, device=dev)
+        vws = torch.empty(fa.fwd_varlen_workspace_bytes(len(lens), total), dtype=torch.uint8, device=dev)
 
         def vcall():
-            fa.fwd_varlen(vq, vk, vv, cu, cu, max(lens), causal=vw["causal"], out=vo, lse=vl)
+            # fa_fwd_varlen_ws: the work-list launch, then the forward over row blocks that hold rows
+            fa.fwd_varlen(vq, vk, vv, cu, cu, causal=vw["causal"], out=vo, lse=vl, workspace=vws)
 
         vms = time_calls(vcall, args.steps, args.warmup, flush)
-        launches += args.steps
+        launches += 2 * args.steps
         vmean = statistics.mean(vms)
         vflops = sum(4.0 * vw["H"] * n * n * vw["d"] / (2.0 if vw["causal"] else 1.0) for n in lens)
-        varlen = {"workload": vw["name"], "lengths": lens, "total_tokens": total, "ms_per_call": vmean,
+        varlen = {"workload": vw["name"], "entry_point": "fa_fwd_varlen_ws", "launches_per_call": 2,
+                  "lengths": lens, "total_tokens": total, "ms_per_call": vmean,
                   "value": sum_over_ranks(vflops, world) / (max_over_ranks(vmean, world) * 1e-3) / 1e12,
                   "unit": "TFLOP/s", "flops_per_call": vflops,
                   "roofline": {"bound": "tensor", "achieved": vflops / (vmean * 1e-3) / 1e12,

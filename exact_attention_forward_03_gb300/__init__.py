@@ -46,7 +46,7 @@ EXPORTS = ("fa_fwd", "fa_fwd_splitkv", "fa_splitkv_combine", "fa_splitkv_workspa
            "fa_version", "fa_fwd_splitkv_noalloc", "fa_splitkv_noalloc_capacity_bytes", "fa_fwd_gqa",
            "fa_fwd_splitkv_gqa", "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace_bytes", "fa_last_error", "fa_fp8_quantize", "fa_fwd_fp8", "fa_selftest_timeout", "fa_bwd_gqa",
            "fa_bwd_varlen", "fa_bwd_varlen_workspace_bytes", "fa_fwd_host",
-           "fa_fwd_host_workspace_bytes")
+           "fa_fwd_host_workspace_bytes", "fa_fwd_varlen_ws", "fa_fwd_varlen_workspace_bytes")
 
 _lock = threading.Lock()
 _lib = None
@@ -101,6 +101,10 @@ def load_library(path: str | None = None):
         lib.fa_fwd_splitkv_gqa.restype = i
         lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_varlen.restype = i
+        lib.fa_fwd_varlen_ws.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, sz, vp]
+        lib.fa_fwd_varlen_ws.restype = i
+        lib.fa_fwd_varlen_workspace_bytes.argtypes = [i, i]
+        lib.fa_fwd_varlen_workspace_bytes.restype = sz
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
         lib.fa_bwd.restype = i
         lib.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, sz, vp]
@@ -366,13 +370,22 @@ def fwd_fp8_from(q, k, v, causal: bool = False, scale: float | None = None, stre
     return fwd_fp8(q8, qs, k8, ks, v8t, vs, causal=causal, scale=scale, out_dtype=q.dtype, stream=stream)
 
 
-def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal: bool = False,
-               scale: float | None = None, out=None, lse=None, want_lse: bool = True, stream=None):
-    """Variable-length (packed) batch through ``fa_fwd_varlen``.
+def fwd_varlen_workspace_bytes(num_seqs: int, total_q: int) -> int:
+    return int(load_library().fa_fwd_varlen_workspace_bytes(num_seqs, total_q))
+
+
+def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int | None = None, causal: bool = False,
+               scale: float | None = None, out=None, lse=None, want_lse: bool = True, stream=None,
+               plan: bool = True, workspace=None):
+    """Variable-length (packed) batch.
 
     q: [total_q, H, d], k, v: [total_k, H_kv, d] (H_kv divides H), cu_seqlens_q/k:
     int32 CUDA tensors of num_seqs + 1 offsets.  Returns (o [total_q, H, d],
-    lse [H, total_q]).  ``max_seqlen_q`` must bound every sequence's query length.
+    lse [H, total_q]).  With ``plan`` (the default) this is ``fa_fwd_varlen_ws``:
+    a device-built work list in ``workspace`` (a uint8 CUDA tensor of at least
+    ``fwd_varlen_workspace_bytes`` bytes, allocated here when None) sends CTAs only
+    to row blocks that hold rows.  Without it, ``fa_fwd_varlen``: a grid sized by
+    ``max_seqlen_q``, which must bound every sequence's query length.
     """
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_cuda or t.dim() != 3 or not t.is_contiguous():
@@ -396,9 +409,25 @@ def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal: b
     if lse is None and want_lse:
         lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
     lib = load_library()
+    num_seqs = cu_seqlens_q.numel() - 1
+    if plan:
+        need = fwd_varlen_workspace_bytes(num_seqs, total_q)
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        elif not workspace.is_cuda or workspace.dtype != torch.uint8 or workspace.numel() < need:
+            raise ValueError(f"workspace must be a uint8 CUDA tensor of at least {need} bytes")
+        rc = lib.fa_fwd_varlen_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  lse.data_ptr() if lse is not None else None, cu_seqlens_q.data_ptr(),
+                                  cu_seqlens_k.data_ptr(), num_seqs, total_q, total_k, H, H_kv, d, int(bool(causal)),
+                                  scale, _dtype_code(q), workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+        if rc != FA_OK:
+            raise FaError(rc, "fa_fwd_varlen_ws")
+        return out, lse
+    if max_seqlen_q is None:
+        raise ValueError("the unplanned grid needs max_seqlen_q")
     rc = lib.fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                            lse.data_ptr() if lse is not None else None, cu_seqlens_q.data_ptr(),
-                           cu_seqlens_k.data_ptr(), cu_seqlens_q.numel() - 1, int(max_seqlen_q), total_q, total_k, H,
+                           cu_seqlens_k.data_ptr(), num_seqs, int(max_seqlen_q), total_q, total_k, H,
                            H_kv, d, int(bool(causal)), scale, _dtype_code(q), _stream_handle(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_varlen")

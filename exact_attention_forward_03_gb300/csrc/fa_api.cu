@@ -231,6 +231,8 @@ int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
     a.cu_q = nullptr;
     a.cu_k = nullptr;
     a.total_q = 0;
+    a.work = nullptr;
+    a.num_seqs = 0;
     a.causal = causal;
     a.scale_log2 = scale * 1.4426950408889634f;
     cudaError_t e = launch_fwd(d, bf16, tq, tk, tv, to, a, BH, reinterpret_cast<cudaStream_t>(stream));
@@ -361,9 +363,59 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *l
     a.cu_q = cu_seqlens_q;
     a.cu_k = cu_seqlens_k;
     a.total_q = total_q;
+    a.work = nullptr;
+    a.num_seqs = num_seqs;
     a.causal = causal;
     a.scale_log2 = scale * 1.4426950408889634f;
     cudaError_t e = launch_fwd_varlen(d, bf16, tq, tk, tv, to, a, num_seqs, reinterpret_cast<cudaStream_t>(stream));
+    return launch_status("kernel launch", e);
+}
+
+size_t fa_fwd_varlen_workspace_bytes(int num_seqs, int total_q) {
+    if (num_seqs <= 0 || total_q <= 0) return 0;
+    return 16 + 8 * ((size_t)(total_q + kFwdBr - 1) / kFwdBr + (size_t)num_seqs);
+}
+
+int fa_fwd_varlen_ws(const void *q, const void *k, const void *v, void *o, float *lse, const int *cu_seqlens_q,
+                     const int *cu_seqlens_k, int num_seqs, int total_q, int total_k, int H, int H_kv, int d,
+                     int causal, float scale, fa_dtype dtype, void *workspace, size_t workspace_bytes,
+                     fa_stream_t stream) {
+    int rc = check_common(q, k, v, o, lse, 1, H, total_q, total_k, d, causal, scale, dtype);
+    if (rc != FA_OK) return rc;
+    if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return FA_ERR_INVALID_ARG;
+    if (!aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4)) return FA_ERR_MISALIGNED;
+    if (num_seqs <= 0 || H_kv <= 0 || H % H_kv != 0 || H > 65535) return FA_ERR_INVALID_ARG;
+    const long long capacity = (long long)(total_q + kFwdBr - 1) / kFwdBr + num_seqs;
+    if (capacity > INT_MAX) return FA_ERR_INVALID_ARG;
+    const size_t need = fa_fwd_varlen_workspace_bytes(num_seqs, total_q);
+    if (workspace == nullptr || !aligned(workspace, 16) || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    DeviceState *st = nullptr;
+    if ((rc = dev_state(&st)) != FA_OK) return rc;
+    const bool bf16 = dtype == FA_BF16;
+    CUtensorMap tq, tk, tv, to;
+    if (make_map_packed(&tq, q, bf16, d, H, total_q, kFwdBr) != FA_OK ||
+        make_map_packed(&tk, k, bf16, d, H_kv, total_k, kFwdBc) != FA_OK ||
+        make_map_packed(&tv, v, bf16, d, H_kv, total_k, kFwdBc) != FA_OK ||
+        make_map_packed(&to, o, bf16, d, H, total_q, kFwdBr) != FA_OK)
+        return FA_ERR_CUDA;
+    FwdArgs a;
+    a.o = o;
+    a.lse = lse;
+    a.status = st->status;
+    a.Nq = 0;
+    a.Nk = 0;
+    a.num_m = (int)capacity;
+    a.H = H;
+    a.group = H / H_kv;
+    a.cu_q = cu_seqlens_q;
+    a.cu_k = cu_seqlens_k;
+    a.total_q = total_q;
+    a.work = nullptr;
+    a.num_seqs = num_seqs;
+    a.causal = causal;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    cudaError_t e = launch_fwd_varlen_planned(d, bf16, tq, tk, tv, to, a, static_cast<int *>(workspace), (int)capacity,
+                                              reinterpret_cast<cudaStream_t>(stream));
     return launch_status("kernel launch", e);
 }
 

@@ -261,19 +261,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int lane = threadIdx.x & 31;
     // Consecutive CTAs take consecutive row blocks of one head, heaviest causal
     // block first, so the CTAs resident at any time share a few heads' K/V in L2.
-    const int bh = blockIdx.y;
+    int bh = blockIdx.y;
     const int causal = args.causal;
     int q0, Nq, Nk, kvh;
     int q_tok = 0, k_tok = 0;  // VARLEN: first token of this sequence in q and in k, v
     if constexpr (VARLEN) {
-        const int seq = bh / args.H;
+        int seq, blk = -1;
+        if (args.work != nullptr) {
+            // Planned grid: blockIdx.x indexes the work list, blockIdx.y is the head.
+            if ((int)blockIdx.x >= args.work[0]) return;  // past the list (the whole CTA)
+            const int2 w = reinterpret_cast<const int2 *>(args.work + 2)[blockIdx.x];
+            seq = w.x;
+            blk = w.y;
+            bh = seq * args.H + (int)blockIdx.y;
+        } else {
+            seq = bh / args.H;
+        }
         q_tok = args.cu_q[seq];
         k_tok = args.cu_k[seq];
         Nq = args.cu_q[seq + 1] - q_tok;
         Nk = args.cu_k[seq + 1] - k_tok;
         const int num_m = (Nq + kFwdBr - 1) / kFwdBr;
-        // Row blocks past this sequence's own ones hold no row: q0 >= Nq gives n = 0.
-        q0 = (int)blockIdx.x < num_m ? (num_m - 1 - (int)blockIdx.x) * kFwdBr : max(Nq, 0);
+        // Unplanned grid: row blocks past this sequence's own ones hold no row (q0 >= Nq).
+        if (blk < 0) blk = (int)blockIdx.x < num_m ? num_m - 1 - (int)blockIdx.x : -1;
+        q0 = blk >= 0 ? blk * kFwdBr : max(Nq, 0);
         kvh = (bh % args.H) / args.group;  // K/V head index within the token's heads
     } else {
         q0 = (args.num_m - 1 - (int)blockIdx.x) * kFwdBr;
@@ -591,6 +602,49 @@ cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMa
 cudaError_t launch_fwd_varlen(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                               const CUtensorMap &to, const FwdArgs &a, int num_seqs, cudaStream_t stream) {
     return launch_fwd_any<true>(d, bf16, tq, tk, tv, to, a, num_seqs * a.H, stream);
+}
+
+// Work list of a variable-length batch (one CTA of 1024 threads).  Sequence s has
+// nb_s = ceil(len_q(s) / 128) row blocks; the sequences are ordered by nb_s
+// descending (ties by index) and each sequence's blocks last-first, the causal
+// heaviest first, so that the longest work starts first.  Each thread finds its
+// sequences' place in that order with one pass over all the block counts
+// (num_seqs^2 / 1024 steps per thread).
+__global__ void __launch_bounds__(1024) fa_fwd_varlen_plan_kernel(const int *cu_q, int num_seqs, int *work) {
+    int2 *list = reinterpret_cast<int2 *>(work + 2);
+    int total = 0;
+    for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
+        const int nb = (cu_q[s + 1] - cu_q[s] + kFwdBr - 1) / kFwdBr;
+        int start = 0;
+        for (int t = 0; t < num_seqs; ++t) {
+            const int nt = (cu_q[t + 1] - cu_q[t] + kFwdBr - 1) / kFwdBr;
+            if (nt > nb || (nt == nb && t < s)) start += nt;
+        }
+        for (int b = 0; b < nb; ++b) list[start + b] = make_int2(s, nb - 1 - b);
+        total += nb;
+    }
+    // the list's length: the sum of every thread's block counts
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+    __shared__ int warp_total[32];
+    if ((threadIdx.x & 31) == 0) warp_total[threadIdx.x >> 5] = total;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int sum = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) sum += warp_total[w];
+        work[0] = sum;
+    }
+}
+
+cudaError_t launch_fwd_varlen_planned(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
+                                     const CUtensorMap &tv, const CUtensorMap &to, const FwdArgs &a, int *work,
+                                     int capacity, cudaStream_t stream) {
+    cudaError_t e = launch_kernel(fa_fwd_varlen_plan_kernel, dim3(1), dim3(1024), 0, stream, a.cu_q, a.num_seqs, work);
+    if (e != cudaSuccess) return e;
+    FwdArgs b = a;
+    b.work = work;
+    b.num_m = capacity;
+    return launch_fwd_any<true>(d, bf16, tq, tk, tv, to, b, a.H, stream);
 }
 
 }  // namespace fa

@@ -34,6 +34,11 @@ struct FwdArgs {
     const int *cu_q;
     const int *cu_k;
     int total_q;    // tokens in the packed q (the lse layout is [H, total_q])
+    // Planned variable-length launches: work[0] = number of row blocks with rows, then
+    // (sequence, row block) pairs from work[2] on, longest sequences first and each
+    // sequence's heaviest (last) row block first; null for the unplanned grid.
+    const int *work;
+    int num_seqs;
     int causal;
     float scale_log2;  // scale * log2(e)
 };
@@ -117,6 +122,12 @@ cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMa
 // y = head, z = token), a.cu_q / a.cu_k set.
 cudaError_t launch_fwd_varlen(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                               const CUtensorMap &to, const FwdArgs &a, int num_seqs, cudaStream_t stream);
+// Planned form: one launch writes the work list (at most `capacity` = ceil(total_q /
+// 128) + num_seqs pairs) into `work`, then the forward runs on a grid of
+// (capacity, H) CTAs, CTAs past the list's end leaving at entry.
+cudaError_t launch_fwd_varlen_planned(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
+                                     const CUtensorMap &tv, const CUtensorMap &to, const FwdArgs &a, int *work,
+                                     int capacity, cudaStream_t stream);
 cudaError_t launch_splitkv(int d, bool bf16, const CUtensorMap &tk, const CUtensorMap &tv, const SplitArgs &a,
                            cudaStream_t stream);
 cudaError_t launch_combine(int d, bool bf16, const CombineArgs &a, cudaStream_t stream);

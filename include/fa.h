@@ -175,6 +175,30 @@ FA_API int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, f
            const int *cu_seqlens_q, const int *cu_seqlens_k, int num_seqs, int max_seqlen_q,
            int total_q, int total_k, int H, int H_kv, int d, int causal, float scale,
            fa_dtype dtype, fa_stream_t stream);
+/*
+ * The same variable-length forward launched over a work list instead of a
+ * (max_seqlen_q / 128) x (num_seqs * H) grid: a first launch on `stream` reads
+ * cu_seqlens_q on the device and writes into `workspace` the (sequence, row
+ * block) pairs that hold rows, longest sequences first and each sequence's
+ * heaviest causal row block first; the forward then runs one CTA per pair and
+ * head, so no CTA is spent on row blocks past a sequence's end and no
+ * max_seqlen_q is needed.  Results are bit for bit those of fa_fwd_varlen.
+ * ("02 · FA2" §2: the sequence dimension as a unit of parallel work; "Lecture
+ * 25" §7.2 item 2: packing without padding.)
+ * Workspace: device memory of at least fa_fwd_varlen_workspace_bytes(num_seqs,
+ * total_q) = 16 + 8 * (ceil(total_q / 128) + num_seqs) bytes, 16-byte aligned,
+ * owned by the caller and free for reuse once the call's work on `stream` has
+ * finished.  The work list is built by one CTA in num_seqs^2 / 1024 steps per
+ * thread, small next to the attention itself for any practical batch.
+ * Errors: as fa_fwd_varlen (without the max_seqlen_q checks; H > 65535 is
+ * FA_ERR_INVALID_ARG), and FA_ERR_WORKSPACE for a null, misaligned or short
+ * workspace.
+ */
+FA_API size_t fa_fwd_varlen_workspace_bytes(int num_seqs, int total_q);
+FA_API int fa_fwd_varlen_ws(const void *q, const void *k, const void *v, void *o, float *lse,
+                            const int *cu_seqlens_q, const int *cu_seqlens_k, int num_seqs, int total_q,
+                            int total_k, int H, int H_kv, int d, int causal, float scale, fa_dtype dtype,
+                            void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
 FA_API int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
            int B, int H, int H_kv, int Nq, int Nk, int d, int causal, float scale,

@@ -63,6 +63,27 @@ def test_validation_without_gpu(lib):
     assert c(p, p, p, None, 4, 1, 1, 1, 32, 0, None) == -2
 
 
+def test_planned_varlen_validation_without_gpu(lib):
+    """fa_fwd_varlen_ws: workspace size formula and argument checks, before any CUDA call."""
+    import exact_attention_forward_03_gb300 as fa
+
+    fa.load_library()
+    assert lib.fa_fwd_varlen_workspace_bytes(16, 10000) == 16 + 8 * (79 + 16)
+    assert lib.fa_fwd_varlen_workspace_bytes(1, 1) == 16 + 8 * 2
+    assert lib.fa_fwd_varlen_workspace_bytes(0, 10) == 0 and lib.fa_fwd_varlen_workspace_bytes(3, 0) == 0
+    p = ctypes.c_void_p(1 << 20)
+    need = lib.fa_fwd_varlen_workspace_bytes(2, 30)
+    f = lib.fa_fwd_varlen_ws
+    args = lambda ws, nbytes, nseq=2, H=2, H_kv=2: (p, p, p, p, None, p, p, nseq, 30, 30, H, H_kv, 64, 0, 0.125, 1,
+                                                      ws, nbytes, None)
+    assert f(*args(None, need)) == fa.FA_ERR_WORKSPACE                              # no workspace
+    assert f(*args(p, need - 8)) == fa.FA_ERR_WORKSPACE                             # one pair short
+    assert f(*args(ctypes.c_void_p((1 << 20) + 8), need)) == fa.FA_ERR_WORKSPACE   # not 16-byte aligned
+    assert f(*args(p, need, nseq=0)) == fa.FA_ERR_INVALID_ARG                       # no sequence
+    assert f(*args(p, need, H=3, H_kv=2)) == fa.FA_ERR_INVALID_ARG                 # H_kv does not divide H
+    assert f(p, p, p, p, None, None, p, 2, 30, 30, 2, 2, 64, 0, 0.125, 1, p, need, None) == fa.FA_ERR_INVALID_ARG
+
+
 def test_gqa_head_counts_are_checked_without_gpu(lib):
     """H must be a positive multiple of H_kv; checked before any CUDA call."""
     p = ctypes.c_void_p(1 << 20)
