@@ -315,7 +315,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
     int *status = args.status;
 
-    if (threadIdx.x == 0) {
+    // The producer's lane initialises the barriers and, before the CTA-wide sync that
+    // waits for the tensor-memory allocation, already sends out the Q tile and the
+    // first K tiles (their slots are fresh, so no empty-slot wait is needed): their
+    // latency overlaps the allocation and the sync.  No other thread touches a
+    // barrier before that sync.
+    constexpr int kProducer = kWarpTma * 32;
+    const int n_first = min(n, 3);  // K tiles loaded before the sync
+    if (threadIdx.x == kProducer) {
         mbar_init(bar(B_QFULL), 1);
         for (int s = 0; s < S_; ++s) {
             mbar_init(bar(B_KFULL(s)), 1);
@@ -338,6 +345,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmO);
+        if (n > 0) {
+            mbar_arrive_expect_tx(bar(B_QFULL), C::kQBytes);
+            for (int b = 0; b < C::kBlocks; ++b)
+                if constexpr (VARLEN)
+                    tma_load_3d(sb + C::kOffQ + b * C::kQBlockBytes, &tmQ, b * 64, bh % args.H, q_tok + q0, bar(B_QFULL));
+                else
+                    tma_load_3d(sb + C::kOffQ + b * C::kQBlockBytes, &tmQ, b * 64, q0, bh, bar(B_QFULL));
+            for (int t = 0; t < n_first; ++t) {
+                mbar_arrive_expect_tx(bar(B_KFULL(t)), C::kTileBytes);
+                for (int b = 0; b < C::kBlocks; ++b)
+                    if constexpr (VARLEN)
+                        tma_load_3d(sb + C::kOffK + t * C::kTileBytes + b * C::kKVBlockBytes, &tmK, b * 64, kvh,
+                                    k_tok + t * kFwdBc, bar(B_KFULL(t)));
+                    else
+                        tma_load_3d(sb + C::kOffK + t * C::kTileBytes + b * C::kKVBlockBytes, &tmK, b * 64,
+                                    t * kFwdBc, kvh, bar(B_KFULL(t)));
+            }
+        }
     }
     if (warp == kWarpPv) {
         tmem_alloc(sb + C::kOffMisc, C::kTmemCols);
@@ -352,14 +377,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (warp == kWarpTma) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && n > 0) {
-            uint32_t pend_k = 0, pend_v = 0;  // slots with a load issued, per ring
-            uint32_t par_k = 0, par_v = 0;    // phase parity of the last load into each slot
-            mbar_arrive_expect_tx(bar(B_QFULL), C::kQBytes);
-            for (int b = 0; b < C::kBlocks; ++b)
-                if constexpr (VARLEN)
-                    tma_load_3d(sb + C::kOffQ + b * C::kQBlockBytes, &tmQ, b * 64, bh % args.H, q_tok + q0, bar(B_QFULL));
-                else
-                    tma_load_3d(sb + C::kOffQ + b * C::kQBlockBytes, &tmQ, b * 64, q0, bh, bar(B_QFULL));
+            // The Q tile and K_0 .. K_{n_first-1} went out before the sync (first use of each slot).
+            uint32_t pend_k = (1u << n_first) - 1u, pend_v = 0;  // slots with a load issued, per ring
+            uint32_t par_k = 0, par_v = 0;                        // phase parity of the last load into each slot
             // Tile `tile` of K (V) goes to slot tile % S of its ring, in the order the two
             // MMA streams consume them: K_0, K_1, K_2, then V_j, K_{j+3} for j = 0, 1, ...
             auto load = [&](bool is_v, int tile) -> bool {
@@ -381,7 +401,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 return true;
             };
             bool ok = true;
-            for (int t = 0; ok && t < min(n, 3); ++t) ok = load(false, t);
             for (int j = 0; ok && j < n; ++j) ok = load(true, j) && (j + 3 >= n || load(false, j + 3));
             // Every load issued must land before the CTA may exit.
             volatile int no_abort = 0;
