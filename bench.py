@@ -5,7 +5,8 @@ Default workload: causal attention forward, B=2, H=32, Nq=Nk=8192, d=128,
 bf16 inputs drawn N(0,1) from fixed seeds, scale 1/sqrt(d).  The headline
 `value` is its throughput in TFLOP/s, counting 4*B*H*Nq*Nk*d FLOPs halved for
 causal, timed with CUDA events around every fa_fwd launch on the launching
-stream, with the L2 cache flushed (a 256 MiB write) before each timed launch.
+stream, with the L2 cache flushed (a 256 MiB write) before each timed launch and
+the device kept busy (a ~0.1 ms spin) while the host enqueues it.
 The split-KV decode path (B=32, H=32, Nq=1, Nk=16384, d=128, bf16, 16 splits)
 is timed the same way and reported under "decode" in GB/s, and its grouped-query
 form (32 query heads over 8 K/V heads) under "decode_gqa".  A packed batch of 16
@@ -186,8 +187,18 @@ def device_uuid():
         return None
 
 
+HOLD_CYCLES = 200_000  # ~0.1 ms of device time
+
+
 def time_calls(fn, steps: int, warmup: int, flush: torch.Tensor | None):
-    """Per-call device milliseconds of fn() with CUDA events on the current stream."""
+    """Per-call device milliseconds of fn() with CUDA events on the current stream.
+
+    With `flush`, every timed call is preceded by an L2 flush (a 256 MiB write) and
+    a short device-side spin (torch.cuda._sleep): the device is busy while the host
+    enqueues the start event and the call, so the interval between the events holds
+    the call's own kernels and no host-side launch gap.  Without `flush` (the
+    end-to-end timing) the interval is whatever the call costs, host work included.
+    """
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         fn()
@@ -196,6 +207,7 @@ def time_calls(fn, steps: int, warmup: int, flush: torch.Tensor | None):
     for e0, e1 in evs:
         if flush is not None:
             flush.fill_(1)  # evicts the previous call's lines from L2
+            torch.cuda._sleep(HOLD_CYCLES)
         e0.record(stream)
         fn()
         e1.record(stream)
