@@ -441,7 +441,7 @@ def run_fa(args, rank, world, local):
             # the backward of the same packed batch (fa_bwd_varlen: plan, preprocess, main kernel, dQ conversion)
             vg = attn_inputs.make_dout(1, total, vw["H"], vw["d"], vw["dtype"], vw["seed"], dev)[0]
             vdq, vdk, vdv = torch.empty_like(vq), torch.empty_like(vk), torch.empty_like(vv)
-            vws = torch.empty(fa.bwd_varlen_workspace_bytes(len(lens), total, vw["H"], vw["d"]), dtype=torch.uint8,
+            vws = torch.empty(fa.bwd_varlen_workspace_bytes(len(lens), total, total, vw["H"], vw["d"]), dtype=torch.uint8,
                               device=dev)
             vcall()
 
@@ -450,10 +450,10 @@ def run_fa(args, rank, world, local):
                               workspace=vws)
 
             vbms = time_calls(vbcall, args.steps, args.warmup, flush)
-            launches += 4 * args.steps
+            launches += 5 * args.steps
             vbmean = statistics.mean(vbms)
             vbflops = 2.5 * vflops
-            varlen_bwd = {"workload": vw["name"], "entry_point": "fa_bwd_varlen", "launches_per_call": 4,
+            varlen_bwd = {"workload": vw["name"], "entry_point": "fa_bwd_varlen", "launches_per_call": 5,
                           "ms_per_call": vbmean,
                           "value": sum_over_ranks(vbflops, world) / (max_over_ranks(vbmean, world) * 1e-3) / 1e12,
                           "unit": "TFLOP/s", "flops_per_call": vbflops,
@@ -461,7 +461,7 @@ def run_fa(args, rank, world, local):
                                        "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                        "frac": vbflops / (vbmean * 1e-3) / 1e12 / peaks["bf16_tflops"],
                                        "traffic": None,
-                                       "note": "whole call (four launches) timed; FLOPs 2.5x the forward's"}}
+                                       "note": "whole call (five launches) timed; FLOPs 2.5x the forward's"}}
             if fa.get_device_status() != fa.FA_OK:
                 raise RuntimeError("device status not ok after the variable-length backward")
             del vg, vdq, vdk, vdv, vws

@@ -114,7 +114,7 @@ def load_library(path: str | None = None):
         lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp,
                                       sz, vp]
         lib.fa_bwd_varlen.restype = i
-        lib.fa_bwd_varlen_workspace_bytes.argtypes = [i, i, i, i]
+        lib.fa_bwd_varlen_workspace_bytes.argtypes = [i, i, i, i, i]
         lib.fa_bwd_varlen_workspace_bytes.restype = sz
         lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, vp, sz, vp]
         lib.fa_fwd_host.restype = i
@@ -434,8 +434,8 @@ def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int | None = N
     return out, lse
 
 
-def bwd_varlen_workspace_bytes(num_seqs, total_q, H, d) -> int:
-    return int(load_library().fa_bwd_varlen_workspace_bytes(num_seqs, total_q, H, d))
+def bwd_varlen_workspace_bytes(num_seqs, total_q, total_k, H, d) -> int:
+    return int(load_library().fa_bwd_varlen_workspace_bytes(num_seqs, total_q, total_k, H, d))
 
 
 def bwd_varlen(q, k, v, o, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_k: int, causal: bool = False,
@@ -471,7 +471,7 @@ def bwd_varlen(q, k, v, o, dout, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_k: 
         outs.append(t)
     dq, dk, dv = outs
     num_seqs = cu_seqlens_q.numel() - 1
-    need = bwd_varlen_workspace_bytes(num_seqs, total_q, H, d)
+    need = bwd_varlen_workspace_bytes(num_seqs, total_q, total_k, H, d)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     rc = load_library().fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),

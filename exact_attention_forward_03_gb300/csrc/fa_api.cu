@@ -633,11 +633,17 @@ static size_t varlen_rows_pad(int num_seqs, int total_q) {
     return (size_t)kBwdBr * ((size_t)(total_q + kBwdBr - 1) / kBwdBr + (size_t)num_seqs);
 }
 
-size_t fa_bwd_varlen_workspace_bytes(int num_seqs, int total_q, int H, int d) {
-    if (num_seqs <= 0 || total_q <= 0 || H <= 0 || (d != 64 && d != 128)) return 0;
+// Key blocks of a packed batch's backward work list: one per 128 keys of each
+// sequence, at most ceil(total_k / 128) + num_seqs.
+static long long bwd_varlen_capacity(int num_seqs, int total_k) {
+    return (long long)(total_k + kBwdBc - 1) / kBwdBc + num_seqs;
+}
+
+size_t fa_bwd_varlen_workspace_bytes(int num_seqs, int total_q, int total_k, int H, int d) {
+    if (num_seqs <= 0 || total_q <= 0 || total_k <= 0 || H <= 0 || (d != 64 && d != 128)) return 0;
     const size_t rows = (size_t)H * varlen_rows_pad(num_seqs, total_q);
     return align256((size_t)(num_seqs + 1) * sizeof(int)) + align256(rows * d * sizeof(float)) +
-           2 * align256(rows * sizeof(float));
+           2 * align256(rows * sizeof(float)) + align256(16 + 8 * (size_t)bwd_varlen_capacity(num_seqs, total_k));
 }
 
 int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse,
@@ -652,9 +658,9 @@ int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, co
     if (!aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4)) return FA_ERR_MISALIGNED;
     if (num_seqs <= 0 || max_seqlen_k <= 0 || max_seqlen_k > total_k) return FA_ERR_INVALID_ARG;
     if (H_kv <= 0 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
-    if ((long long)num_seqs * H_kv > 65535) return FA_ERR_INVALID_ARG;  // grid.y limit
+    if (H_kv > 65535 || bwd_varlen_capacity(num_seqs, total_k) > INT_MAX) return FA_ERR_INVALID_ARG;  // grid limits
     if ((long long)H * (long long)varlen_rows_pad(num_seqs, total_q) > INT_MAX) return FA_ERR_INVALID_ARG;
-    const size_t need = fa_bwd_varlen_workspace_bytes(num_seqs, total_q, H, d);
+    const size_t need = fa_bwd_varlen_workspace_bytes(num_seqs, total_q, total_k, H, d);
     if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need) return FA_ERR_WORKSPACE;
     DeviceState *st = nullptr;
     if ((rc = dev_state(&st)) != FA_OK) return rc;
@@ -682,6 +688,8 @@ int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, co
     a.lse2 = reinterpret_cast<float *>(ws);
     ws += align256(rows * sizeof(float));
     a.dvec = reinterpret_cast<float *>(ws);
+    ws += align256(rows * sizeof(float));
+    int *work = reinterpret_cast<int *>(ws);  // the key-block work list
     a.status = st->status;
     a.BH = H;  // query heads per token
     a.H = H;
@@ -694,7 +702,8 @@ int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, co
     a.num_seqs = num_seqs;
     a.total_q = total_q;
     a.rows_pad = (int)rows_pad;
-    cudaError_t e = launch_bwd_varlen(d, bf16, tq, tk, tv, tdo, a, max_seqlen_k, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_bwd_varlen(d, bf16, tq, tk, tv, tdo, a, work, (int)bwd_varlen_capacity(num_seqs, total_k),
+                                      reinterpret_cast<cudaStream_t>(stream));
     return launch_status("kernel launch", e);
 }
 

@@ -128,13 +128,14 @@ __device__ __forceinline__ void bwd_p_chunk(const uint32_t (&sv)[32], const floa
     }
 }
 
-// VARLEN: a packed variable-length batch.  blockIdx.y = sequence * H_kv + K/V head;
+// VARLEN: a packed variable-length batch.  blockIdx.x indexes a work list of
+// (sequence, key block) pairs (longest sequences first), blockIdx.y is the K/V head;
 // q, o, dO are [total_q, H, d], k, v, dK, dV are [total_k, H_kv, d] (tensor maps
 // indexed by column, head, token), and sequence s spans tokens [cu_q[s], cu_q[s+1])
 // of q and [cu_k[s], cu_k[s+1]) of k and v.  A query block may run past its
 // sequence into the next one's tokens: those rows' padded LSE entries are -inf, so
 // they get P = 0 and add nothing; keys past the sequence are masked like a ragged
-// K tail.  A CTA whose key block lies past its sequence's keys leaves at entry.
+// K tail.  A CTA past the end of the work list leaves at entry.
 template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -154,13 +155,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int k0 = blockIdx.x * kBwdBc;  // first key of this block (block 0 has the most work when causal)
+    int k0 = blockIdx.x * kBwdBc;  // first key of this block (block 0 has the most work when causal)
     const int causal = args.causal;
     const int H_kv = args.H / args.group;
     int Nq, Nk, bhk, bh0, ld_rows, seq_off, q_tok = 0, k_tok = 0;
     if constexpr (VARLEN) {
-        const int seq = blockIdx.y / H_kv;
-        bhk = blockIdx.y % H_kv;               // K/V head within a token
+        if ((int)blockIdx.x >= args.work[0]) return;  // past the list: the whole CTA, nothing touched yet
+        const int2 w = reinterpret_cast<const int2 *>(args.work + 2)[blockIdx.x];
+        const int seq = w.x;
+        k0 = w.y * kBwdBc;
+        bhk = blockIdx.y;                      // K/V head within a token
         q_tok = args.cu_q[seq];
         k_tok = args.cu_k[seq];
         Nq = args.cu_q[seq + 1] - q_tok;
@@ -716,11 +720,16 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const BwdArgs a) {
 
 template <int D, bool BF16, bool VARLEN>
 static cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                                const CUtensorMap &tdo, const BwdArgs &a, int max_seqlen_k, cudaStream_t stream) {
+                                const CUtensorMap &tdo, const BwdArgs &a_in, int *work, int capacity,
+                                cudaStream_t stream) {
+    BwdArgs a = a_in;
+    a.work = work;
     using C = BwdCfg<D>;
     cudaError_t e;
     if constexpr (VARLEN) {
         e = launch_kernel(fa_bwd_plan_kernel, dim3(1), dim3(32), 0, stream, a);
+        if (e != cudaSuccess) return e;
+        e = launch_varlen_plan(a.cu_k, a.num_seqs, work, false, stream);
         if (e != cudaSuccess) return e;
     }
     const long long rows = (long long)a.BH * (VARLEN ? a.rows_pad : a.Nq_pad);
@@ -731,7 +740,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, co
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int H_kv = a.H / a.group;
-    const dim3 grid = VARLEN ? dim3((unsigned)((max_seqlen_k + kBwdBc - 1) / kBwdBc), (unsigned)(a.num_seqs * H_kv), 1)
+    const dim3 grid = VARLEN ? dim3((unsigned)capacity, (unsigned)H_kv, 1)
                              : dim3((unsigned)((a.Nk + kBwdBc - 1) / kBwdBc), (unsigned)(a.BH / a.group), 1);
     e = launch_kernel(kern, grid, dim3(kBwdThreads), C::kSmemBytes, stream, tq, tk, tv, tdo, a);
     if (e != cudaSuccess) return e;
@@ -742,18 +751,18 @@ static cudaError_t launch_bwd_t(const CUtensorMap &tq, const CUtensorMap &tk, co
 
 cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream) {
-    if (d == 64) return bf16 ? launch_bwd_t<64, true, false>(tq, tk, tv, tdo, a, 0, stream)
-                             : launch_bwd_t<64, false, false>(tq, tk, tv, tdo, a, 0, stream);
-    return bf16 ? launch_bwd_t<128, true, false>(tq, tk, tv, tdo, a, 0, stream)
-                : launch_bwd_t<128, false, false>(tq, tk, tv, tdo, a, 0, stream);
+    if (d == 64) return bf16 ? launch_bwd_t<64, true, false>(tq, tk, tv, tdo, a, nullptr, 0, stream)
+                             : launch_bwd_t<64, false, false>(tq, tk, tv, tdo, a, nullptr, 0, stream);
+    return bf16 ? launch_bwd_t<128, true, false>(tq, tk, tv, tdo, a, nullptr, 0, stream)
+                : launch_bwd_t<128, false, false>(tq, tk, tv, tdo, a, nullptr, 0, stream);
 }
 
 cudaError_t launch_bwd_varlen(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                              const CUtensorMap &tdo, const BwdArgs &a, int max_seqlen_k, cudaStream_t stream) {
-    if (d == 64) return bf16 ? launch_bwd_t<64, true, true>(tq, tk, tv, tdo, a, max_seqlen_k, stream)
-                             : launch_bwd_t<64, false, true>(tq, tk, tv, tdo, a, max_seqlen_k, stream);
-    return bf16 ? launch_bwd_t<128, true, true>(tq, tk, tv, tdo, a, max_seqlen_k, stream)
-                : launch_bwd_t<128, false, true>(tq, tk, tv, tdo, a, max_seqlen_k, stream);
+                              const CUtensorMap &tdo, const BwdArgs &a, int *work, int capacity, cudaStream_t stream) {
+    if (d == 64) return bf16 ? launch_bwd_t<64, true, true>(tq, tk, tv, tdo, a, work, capacity, stream)
+                             : launch_bwd_t<64, false, true>(tq, tk, tv, tdo, a, work, capacity, stream);
+    return bf16 ? launch_bwd_t<128, true, true>(tq, tk, tv, tdo, a, work, capacity, stream)
+                : launch_bwd_t<128, false, true>(tq, tk, tv, tdo, a, work, capacity, stream);
 }
 
 }  // namespace fa

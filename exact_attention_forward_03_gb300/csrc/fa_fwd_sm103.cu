@@ -624,22 +624,23 @@ cudaError_t launch_fwd_varlen(int d, bool bf16, const CUtensorMap &tq, const CUt
 }
 
 // Work list of a variable-length batch (one CTA of 1024 threads).  Sequence s has
-// nb_s = ceil(len_q(s) / 128) row blocks; the sequences are ordered by nb_s
-// descending (ties by index) and each sequence's blocks last-first, the causal
-// heaviest first, so that the longest work starts first.  Each thread finds its
-// sequences' place in that order with one pass over all the block counts
-// (num_seqs^2 / 1024 steps per thread).
-__global__ void __launch_bounds__(1024) fa_fwd_varlen_plan_kernel(const int *cu_q, int num_seqs, int *work) {
+// nb_s = ceil(len(s) / 128) blocks of 128 tokens; the sequences are ordered by nb_s
+// descending (ties by index) and each sequence's blocks last-first (the forward's
+// heaviest causal row block is its last) or first-first (the backward's heaviest
+// causal key block is its first), so that the longest work starts first.  Each
+// thread finds its sequences' place in that order with one pass over all the block
+// counts (num_seqs^2 / 1024 steps per thread).
+__global__ void __launch_bounds__(1024) fa_varlen_plan_kernel(const int *cu, int num_seqs, int *work, int last_first) {
     int2 *list = reinterpret_cast<int2 *>(work + 2);
     int total = 0;
     for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
-        const int nb = (cu_q[s + 1] - cu_q[s] + kFwdBr - 1) / kFwdBr;
+        const int nb = (cu[s + 1] - cu[s] + kFwdBr - 1) / kFwdBr;
         int start = 0;
         for (int t = 0; t < num_seqs; ++t) {
-            const int nt = (cu_q[t + 1] - cu_q[t] + kFwdBr - 1) / kFwdBr;
+            const int nt = (cu[t + 1] - cu[t] + kFwdBr - 1) / kFwdBr;
             if (nt > nb || (nt == nb && t < s)) start += nt;
         }
-        for (int b = 0; b < nb; ++b) list[start + b] = make_int2(s, nb - 1 - b);
+        for (int b = 0; b < nb; ++b) list[start + b] = make_int2(s, last_first ? nb - 1 - b : b);
         total += nb;
     }
     // the list's length: the sum of every thread's block counts
@@ -655,10 +656,14 @@ __global__ void __launch_bounds__(1024) fa_fwd_varlen_plan_kernel(const int *cu_
     }
 }
 
+cudaError_t launch_varlen_plan(const int *cu, int num_seqs, int *work, bool last_first, cudaStream_t stream) {
+    return launch_kernel(fa_varlen_plan_kernel, dim3(1), dim3(1024), 0, stream, cu, num_seqs, work, last_first ? 1 : 0);
+}
+
 cudaError_t launch_fwd_varlen_planned(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
                                      const CUtensorMap &tv, const CUtensorMap &to, const FwdArgs &a, int *work,
                                      int capacity, cudaStream_t stream) {
-    cudaError_t e = launch_kernel(fa_fwd_varlen_plan_kernel, dim3(1), dim3(1024), 0, stream, a.cu_q, a.num_seqs, work);
+    cudaError_t e = launch_varlen_plan(a.cu_q, a.num_seqs, work, true, stream);
     if (e != cudaSuccess) return e;
     FwdArgs b = a;
     b.work = work;

@@ -91,6 +91,11 @@ struct BwdArgs {
     const int *cu_q, *cu_k;
     int *row_off;
     int num_seqs, total_q, rows_pad;
+    // Work list of the main kernel's CTAs (packed batches): work[0] = number of
+    // (sequence, key block) pairs with keys, the pairs from work[2] on, longest
+    // sequences first and each sequence's key blocks in ascending order (key block 0
+    // sees the most query blocks under the causal mask).  Null for dense.
+    const int *work;
 };
 
 // FP8 (E4M3) forward: blocks of 128 rows of one head carry one fp32 scale each.
@@ -125,6 +130,12 @@ cudaError_t launch_fwd_varlen(int d, bool bf16, const CUtensorMap &tq, const CUt
 // Planned form: one launch writes the work list (at most `capacity` = ceil(total_q /
 // 128) + num_seqs pairs) into `work`, then the forward runs on a grid of
 // (capacity, H) CTAs, CTAs past the list's end leaving at entry.
+// Work list of a packed batch from the offsets `cu` (num_seqs + 1 of them): work[0] =
+// the number of 128-token blocks that hold tokens, then (sequence, block) pairs,
+// sequences ordered by block count (descending, ties by index), each sequence's
+// blocks last-first (`last_first`) or first-first.  One CTA; at most
+// ceil(total / 128) + num_seqs pairs.
+cudaError_t launch_varlen_plan(const int *cu, int num_seqs, int *work, bool last_first, cudaStream_t stream);
 cudaError_t launch_fwd_varlen_planned(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
                                      const CUtensorMap &tv, const CUtensorMap &to, const FwdArgs &a, int *work,
                                      int capacity, cudaStream_t stream);
@@ -139,9 +150,10 @@ cudaError_t launch_selftest_timeout(int *status, int limit_ms, cudaStream_t stre
 // Backward: preprocess (D, lse2, zero dq_acc), the main K/V-block kernel, dQ conversion.
 cudaError_t launch_bwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tdo, const BwdArgs &a, cudaStream_t stream);
-// Variable-length form: packed tensor maps (column, head, token), grid
-// (ceil(max_seqlen_k / 128), num_seqs * H_kv); a.cu_q, a.cu_k, a.row_off set.
+// Variable-length form: packed tensor maps (column, head, token), a.cu_q, a.cu_k,
+// a.row_off set, `work` a buffer of 16 + 8 * capacity bytes for the key-block work
+// list (capacity = ceil(total_k / 128) + num_seqs); grid (capacity, H_kv).
 cudaError_t launch_bwd_varlen(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                              const CUtensorMap &tdo, const BwdArgs &a, int max_seqlen_k, cudaStream_t stream);
+                              const CUtensorMap &tdo, const BwdArgs &a, int *work, int capacity, cudaStream_t stream);
 
 }  // namespace fa

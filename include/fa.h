@@ -330,27 +330,31 @@ FA_API int fa_bwd(const void *q, const void *k, const void *v, const void *o, co
  * lengths.  Layouts as in fa_fwd_varlen: q, o, dout, dq packed [total_q, H, d];
  * k, v, dk, dv [total_k, H_kv, d]; lse [H, total_q] fp32 as fa_fwd_varlen wrote
  * it; cu_seqlens_q, cu_seqlens_k DEVICE arrays of num_seqs + 1 int32 offsets with
- * the same guarantees as there.  max_seqlen_k must be at least the longest
- * sequence's key count (the grid is sized by it; keys past it would get no
- * gradient).  Every query token's dq and every key token's dk, dv are written;
+ * the same guarantees as there.  max_seqlen_k must lie in [1, total_k] (it is
+ * checked but no longer sizes the grid: the CTAs follow a work list of the
+ * (sequence, key block) pairs that hold keys, built on the device from
+ * cu_seqlens_k, longest sequences first and each sequence's key blocks in
+ * ascending order, the causal heaviest first).  Every query token's dq and every
+ * key token's dk, dv are written;
  * a sequence without query tokens gets dK = dV = 0, one without keys dQ = 0.
  * Q, K, V and dO must be finite everywhere: a tile may read tokens of the
  * neighbouring sequence and weights them by exactly 0.
- * Workspace: at least fa_bwd_varlen_workspace_bytes(num_seqs, total_q, H, d)
- * bytes, 256-byte aligned, owned by the caller; besides the buffers of fa_bwd it
- * holds each sequence's first row in a per-head row space where sequences start
- * on multiples of 128 rows, computed on the device from cu_seqlens_q.  Four
- * launches on `stream` (that plan, then those of fa_bwd).
+ * Workspace: at least fa_bwd_varlen_workspace_bytes(num_seqs, total_q, total_k,
+ * H, d) bytes, 256-byte aligned, owned by the caller; besides the buffers of
+ * fa_bwd it holds each sequence's first row in a per-head row space where
+ * sequences start on multiples of 128 rows, computed on the device from
+ * cu_seqlens_q, and the work list (16 + 8 * (ceil(total_k / 128) + num_seqs)
+ * bytes).  Five launches on `stream` (the two plans, then those of fa_bwd).
  * ("Flash Attention (4)" §5: the entry with cu_seqlens; "Lecture 25" §3.3: the
  * recomputing backward.)
  * Errors: the common validation (total_q, total_k in the places of Nq, Nk);
  * FA_ERR_INVALID_ARG for a null dout, lse, dq, dk, dv or offset array,
  * num_seqs <= 0, max_seqlen_k outside [1, total_k], H not a multiple of H_kv,
- * or num_seqs * H_kv > 65535; FA_ERR_MISALIGNED for dout, dq, dk, dv not 16-byte
+ * or H_kv > 65535; FA_ERR_MISALIGNED for dout, dq, dk, dv not 16-byte
  * or offsets not 4-byte aligned; FA_ERR_WORKSPACE for a null, misaligned or
  * short workspace.
  */
-FA_API size_t fa_bwd_varlen_workspace_bytes(int num_seqs, int total_q, int H, int d);
+FA_API size_t fa_bwd_varlen_workspace_bytes(int num_seqs, int total_q, int total_k, int H, int d);
 FA_API int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const void *dout,
                          const float *lse, void *dq, void *dk, void *dv, const int *cu_seqlens_q,
                          const int *cu_seqlens_k, int num_seqs, int max_seqlen_k, int total_q, int total_k, int H,

@@ -165,9 +165,11 @@ def test_backward_and_fp8_validation_without_gpu(lib):
     assert vb(*args(dq=odd)) == -3
     assert vb(*args(cu_q=two)) == -3
     assert vb(*args(ws=None)) == -4
-    need = lib.fa_bwd_varlen_workspace_bytes(2, 30, 2, 64)
-    # offsets, then per head 128 (ceil(30 / 128) + 2) rows of 64 floats and two vectors
-    assert need == 256 + 2 * 384 * 64 * 4 + 2 * (2 * 384 * 4)
+    need = lib.fa_bwd_varlen_workspace_bytes(2, 30, 30, 2, 64)
+    # offsets, then per head 128 (ceil(30 / 128) + 2) rows of 64 floats and two vectors, then the
+    # key-block work list: 16 + 8 (ceil(30 / 128) + 2) bytes, rounded up to 256
+    assert need == 256 + 2 * 384 * 64 * 4 + 2 * (2 * 384 * 4) + 256
+    assert lib.fa_bwd_varlen_workspace_bytes(2, 30, 0, 2, 64) == 0
     assert vb(*args(bytes=need - 1)) == -4
     h = lib.fa_fwd_host
     assert h(None, p, p, p, p, 1, 2, 2, 8, 8, 64, 0, 0.1, 1, 0, p, ws, None) == -1       # null q_host

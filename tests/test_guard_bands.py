@@ -88,7 +88,7 @@ def test_packed_variable_length(fa):
     fa.fwd_varlen(q, k, v, cu, cu, max(lens), causal=True, out=o.t, lse=lse.t)
     _check(fa, ("o", o), ("lse", lse))
     dq, dk, dv = Guarded(q.shape, q.dtype), Guarded(k.shape, k.dtype), Guarded(v.shape, v.dtype)
-    ws = Guarded(nbytes=fa.bwd_varlen_workspace_bytes(len(lens), total, H, d))
+    ws = Guarded(nbytes=fa.bwd_varlen_workspace_bytes(len(lens), total, total, H, d))
     fa.bwd_varlen(q, k, v, o.t, dout, lse.t, cu, cu, max(lens), causal=True, dq=dq.t, dk=dk.t, dv=dv.t,
                   workspace=ws.t)
     _check(fa, ("dq", dq), ("dk", dk), ("dv", dv), ("workspace", ws))

@@ -158,7 +158,7 @@ def test_varlen_bwd_rejects_bad_arguments(fa):
     with pytest.raises(fa.FaError) as e:
         fa.bwd_varlen(q, k, v, o, dout, lse, cu_q, cu_k, 31)   # more than total_k
     assert e.value.code == fa.FA_ERR_INVALID_ARG
-    short = torch.empty(fa.bwd_varlen_workspace_bytes(2, 30, 2, 64) - 256, dtype=torch.uint8, device="cuda")
+    short = torch.empty(fa.bwd_varlen_workspace_bytes(2, 30, 30, 2, 64) - 256, dtype=torch.uint8, device="cuda")
     with pytest.raises(fa.FaError) as e:
         fa.bwd_varlen(q, k, v, o, dout, lse, cu_q, cu_k, 20, workspace=short)
     assert e.value.code == fa.FA_ERR_WORKSPACE
