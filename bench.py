@@ -7,7 +7,7 @@ bf16 inputs drawn N(0,1) from fixed seeds, scale 1/sqrt(d).  The headline
 causal, timed with CUDA events around every fa_fwd launch on the launching
 stream, with the L2 cache flushed (a 256 MiB write) before each timed launch and
 the device kept busy (a ~0.1 ms spin) while the host enqueues it.
-The split-KV decode path (B=32, H=32, Nq=1, Nk=16384, d=128, bf16, 16 splits)
+The split-KV decode path (B=32, H=32, Nq=1, Nk=16384, d=128, bf16, 8 splits)
 is timed the same way and reported under "decode" in GB/s, and its grouped-query
 form (32 query heads over 8 K/V heads) under "decode_gqa".  A packed batch of 16
 causal sequences of 256..8192 tokens goes under "varlen" (forward) and
@@ -20,7 +20,7 @@ other workloads is timed the same way and reported with its own roofline under
 "cfg1" / "cfg1_causal" (B=1, H=1, N=128, d=64, fp16: one CTA, a latency case),
 "cfg2" / "cfg2_causal" (B=4, H=16, N=1024, d=64, fp16), "cfg3_noncausal" (the
 default shape without the mask) and "cfg4" (B=1, H=32, N=32768, d=128, bf16,
-causal); the decode workload at 8 and 32 splits under "decode_s8" and
+causal); the decode workload at 16 and 32 splits under "decode_s16" and
 "decode_s32".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fa|reference]
@@ -543,7 +543,7 @@ def run_fa(args, rank, world, local):
         dec_in = attn_inputs.make_workload(wdec, dev)
         decode = measure_decode(wdec, inputs=dec_in)
         launches += 2 * args.steps
-        for sp in (8, 32):  # the split count against the HBM roofline (16 is `decode`)
+        for sp in (8, 16, 32):  # the split count against the HBM roofline (`decode` is --decode-splits)
             if sp != args.decode_splits:
                 configs[f"decode_s{sp}"] = measure_decode(wdec, splits=sp, inputs=dec_in)
                 launches += 2 * args.steps
@@ -646,7 +646,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["fa", "reference"], default="fa")
     ap.add_argument("--workload", default="b2h32_n8192_d128_bf16_causal", choices=sorted(attn_inputs.WORKLOADS))
     ap.add_argument("--decode-workload", default="decode_b32h32_nk16384_d128_bf16")
-    ap.add_argument("--decode-splits", type=int, default=16)
+    ap.add_argument("--decode-splits", type=int, default=8)
     ap.add_argument("--decode-gqa-workload", default="decode_b32h32kv8_nk16384_d128_bf16",
                     help="grouped-query decode workload reported under decode_gqa ('' to skip)")
     ap.add_argument("--no-decode", action="store_true")

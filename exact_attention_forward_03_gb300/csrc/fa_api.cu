@@ -156,9 +156,11 @@ int check_common(const void *q, const void *k, const void *v, const void *o, con
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 int auto_splits(int num_sms, long long rows, int Nk) {
-    // Enough CTAs for about eight waves at two resident CTAs per SM, at least one
-    // 64-key tile per split, at most 64 splits.
-    const long long target = 16LL * (num_sms > 0 ? num_sms : 148);
+    // About 48 CTAs per SM, at least one 64-key tile per split, at most 64 splits.
+    // Measured on GB300 at B=32, H=32, Nk=16384, d=128 (GB/s of compulsory bytes by
+    // split count): 1: 5802, 2: 6580, 3: 6365, 4: 6585, 6: 6600, 8: 6701, 12: 6616,
+    // 16: 6554, 32: 6233; this target picks 8 there.
+    const long long target = 48LL * (num_sms > 0 ? num_sms : 148);
     long long s = (target + rows - 1) / rows;
     const long long tiles = (Nk + kDecBc - 1) / kDecBc;
     if (s > tiles) s = tiles;
