@@ -12,10 +12,12 @@
 //
 // Roles (warp specialisation, 8 warps):
 //   warps 0-3  softmax: one thread per query row (TMEM lane = row), the whole
-//              128-key row of S in registers
+//              128-key row of S in registers; then the epilogue
 //   warp 4     TMA producer: the Q tile once, then K_0, K_1, K_2, V_0, K_3,
 //              V_1, K_4, ... into two rings of shared-memory slots, one for K
-//              tiles and one for V tiles (full/empty mbarriers per slot)
+//              tiles and one for V tiles (full/empty mbarriers per slot).  Its
+//              lane initialises the barriers and issues Q and K_0..K_2 before
+//              the CTA-wide sync on the tensor-memory allocation.
 //   warp 5     owns tensor memory; one lane issues O += P(j) V_j for every j
 //   warp 6     one lane issues S(t) = Q K_t^T for every t
 //   warp 7     idle
@@ -47,6 +49,11 @@
 // Barrier phases: S(t), P(j) and "PV(j) done" each use three barriers indexed
 // by tile mod 3, so that no waiter can fall two phases behind on the barrier
 // it waits on (every pair of producer and consumer is at most two tiles apart).
+//
+// Epilogue: O = O~ / l and LSE per row; the 16-bit O rows are staged in the
+// freed K ring slot 0 in the Q/K tile layout and leave as TMA stores of whole
+// tiles (a packed batch's partial last row block of a sequence is stored row by
+// row instead, since its box would overlap the next sequence's rows).
 //
 // Every mbarrier wait is bounded (%globaltimer); on expiry the CTA records
 // the timeout in the status word, stops issuing work, waits (bounded) for its
