@@ -593,10 +593,15 @@ def run_fa(args, rank, world, local):
         threads = os.cpu_count() or 1
         wide = oracle.WidenedWorkload(q, k, v)  # fp64 host copies, made before the timing
         rate, rows, secs = oracle_rate(w, wide, args.cpu_seconds, threads)
+        rate1, rows1, secs1 = oracle_rate(w, wide, max(1.0, args.cpu_seconds / 4), 1, seed=30_000)
+        oracle.set_threads(threads)
         del wide
         cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"{rows} uniformly sampled query rows of {w.name} (full key range each), {secs:.1f} s "
-                         "of oracle arithmetic (inputs widened to fp64 once, outside the timing)"}
+                         "of oracle arithmetic (inputs widened to fp64 once, outside the timing)",
+               "extrapolated_full_oracle_s": w.flops() / (rate * 1e12),
+               "single_core": {"value": rate1, "unit": "TFLOP/s", "cores": 1, "rows": rows1, "seconds": secs1,
+                               "extrapolated_full_oracle_s": w.flops() / (rate1 * 1e12)}}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

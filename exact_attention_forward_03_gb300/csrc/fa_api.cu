@@ -302,9 +302,21 @@ int fa_fwd_host(const void *q_host, const void *k_host, const void *v_host, void
         (e = cudaStreamWaitEvent(st->copy_in, st->ev_entry, 0)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(st->copy_out, st->ev_entry, 0)) != cudaSuccess)
         return join_and_fail("fa_fwd_host ordering", e);
+    // Chunk c covers K/V heads [bound(c), bound(c+1)).  The copies of all chunks stream
+    // back to back; after the last chunk's inputs arrive only its compute and its output
+    // copy remain, so the last two chunks are tapered to 1/2 and 1/4 of the others
+    // (weights 1, ..., 1, 1/2, 1/4, in quarters), every chunk keeping at least one head.
+    const long long w_total = chunks >= 4 ? 4LL * (chunks - 2) + 3 : chunks;
+    auto bound = [&](int c) -> int {
+        long long w = c;  // equal chunks
+        if (chunks >= 4) w = c <= chunks - 2 ? 4LL * c : 4LL * (chunks - 2) + 2;
+        if (chunks >= 4 && c == chunks) w = w_total;
+        const int h = (int)((long long)kv_heads * w / w_total);
+        return c == 0 ? 0 : (h < c ? c : (h > kv_heads - (chunks - c) ? kv_heads - (chunks - c) : h));
+    };
     for (int c = 0; c < chunks; ++c) {
         // K/V heads [h0, h1) and their query heads [h0 * group, h1 * group)
-        const int h0 = (int)((long long)kv_heads * c / chunks), h1 = (int)((long long)kv_heads * (c + 1) / chunks);
+        const int h0 = bound(c), h1 = bound(c + 1);
         const size_t qo = (size_t)h0 * group * q_head, qn = (size_t)(h1 - h0) * group * q_head;
         const size_t ko = (size_t)h0 * k_head, kn = (size_t)(h1 - h0) * k_head;
         const size_t lo = (size_t)h0 * group * Nq, ln = (size_t)(h1 - h0) * group * Nq;  // lse elements
