@@ -51,9 +51,11 @@
 // it waits on (every pair of producer and consumer is at most two tiles apart).
 //
 // Epilogue: O = O~ / l and LSE per row; the 16-bit O rows are staged in the
-// freed K ring slot 0 in the Q/K tile layout and leave as TMA stores of whole
-// tiles (a packed batch's partial last row block of a sequence is stored row by
-// row instead, since its box would overlap the next sequence's rows).
+// freed K ring slot 0 in the Q/K tile layout, one 64-column block at a time, and
+// each block leaves as a TMA store as soon as all its rows are staged, reading
+// shared memory while the next block is packed (a packed batch's partial last
+// row block of a sequence is stored row by row instead, since its box would
+// overlap the next sequence's rows).
 //
 // Every mbarrier wait is bounded (%globaltimer); on expiry the CTA records
 // the timeout in the status word, stops issuing work, waits (bounded) for its
@@ -532,62 +534,69 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const bool staged = !VARLEN || q0 + kFwdBr <= Nq;
         const bool valid = i < Nq;
         const int row = quarter * 32 + lane;
-        if (ok && __any_sync(0xffffffffu, valid)) {
-            const float inv = (l > 0.f) ? 1.f / l : 0.f;
-            const size_t orow = VARLEN ? (size_t)(q_tok + i) * args.H + bh % args.H : (size_t)bh * Nq + i;
-            typename PK::T *orow_g = reinterpret_cast<typename PK::T *>(args.o) + orow * D;
-            uint8_t *stage_row = smem + C::kOffK + row * 128;
+        const bool work = ok && __any_sync(0xffffffffu, valid);  // the same on the whole warp
+        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+        const size_t orow = VARLEN ? (size_t)(q_tok + i) * args.H + bh % args.H : (size_t)bh * Nq + i;
+        typename PK::T *orow_g = reinterpret_cast<typename PK::T *>(args.o) + orow * D;
+        uint8_t *stage_row = smem + C::kOffK + row * 128;
+        // One 64-column block at a time: once every softmax warp has staged block b,
+        // its TMA store goes out and reads shared memory while the next block is packed.
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t ov[32];
-                if (n > 0) {
-                    tmem_ld_32x32b_x32(o_addr + 32 * c, ov);
-                    tmem_wait_ld();
-                } else {
+        for (int b = 0; b < C::kBlocks; ++b) {
+            if (work) {
+#pragma unroll 1
+                for (int c = 2 * b; c < 2 * b + 2; ++c) {
+                    uint32_t ov[32];
+                    if (n > 0) {
+                        tmem_ld_32x32b_x32(o_addr + 32 * c, ov);
+                        tmem_wait_ld();
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) ov[e] = 0u;
-                }
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = PK::pack(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
-                if (staged) {
-                    // columns [32c, 32c+32): 64-column block c/2, 16-byte chunks 4(c%2)..4(c%2)+3,
-                    // chunk k of row r at r*128 + 16*(k ^ (r mod 8)) (the 128-byte swizzle)
-                    uint8_t *blk = stage_row + (c >> 1) * C::kKVBlockBytes;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int k = 4 * (c & 1) + e;
-                        *reinterpret_cast<uint4 *>(blk + 16 * (k ^ (row & 7))) =
-                            make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                        for (int e = 0; e < 32; ++e) ov[e] = 0u;
                     }
-                } else if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow_g + 32 * c);
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = PK::pack(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+                    if (staged) {
+                        // columns [32c, 32c+32): 64-column block b, 16-byte chunks 4(c%2)..4(c%2)+3,
+                        // chunk k of row r at r*128 + 16*(k ^ (r mod 8)) (the 128-byte swizzle)
+                        uint8_t *blk = stage_row + b * C::kKVBlockBytes;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int k = 4 * (c & 1) + e;
+                            *reinterpret_cast<uint4 *>(blk + 16 * (k ^ (row & 7))) =
+                                make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                        }
+                    } else if (valid) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow_g + 32 * c);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                    }
                 }
             }
-            if (valid && args.lse != nullptr) {
-                const float m_fin = (m == -INFINITY) ? 0.f : m;
-                const size_t lrow = VARLEN ? (size_t)(bh % args.H) * args.total_q + q_tok + i : (size_t)bh * Nq + i;
-                args.lse[lrow] = (l > 0.f) ? m_fin * 0.69314718055994531f + logf(l) : -INFINITY;
-            }
-        }
-        if (staged) {
-            // Every softmax warp arrives (whatever its rows or its wait outcomes), so the
-            // barrier always completes; the stores go out only if no warp gave up a wait.
-            fence_proxy_async_smem();
-            const bool all_ok = named_bar_and(1, 128, ok);
-            if (all_ok && threadIdx.x == 0) {
-                for (int b = 0; b < C::kBlocks; ++b)
+            if (staged) {
+                // Every softmax warp arrives (whatever its rows or its wait outcomes), so the
+                // barrier always completes; the stores go out only if no warp gave up a wait.
+                fence_proxy_async_smem();
+                const bool all_ok = named_bar_and(1, 128, ok);
+                if (all_ok && threadIdx.x == 0) {
                     if constexpr (VARLEN)
                         tma_store_3d(&tmO, sb + C::kOffK + b * C::kKVBlockBytes, b * 64, bh % args.H, q_tok + q0);
                     else
                         tma_store_3d(&tmO, sb + C::kOffK + b * C::kKVBlockBytes, b * 64, q0, bh);
-                bulk_commit();
-                bulk_wait_read();
+                    bulk_commit();
+                }
             }
         }
+        if (work && valid && args.lse != nullptr) {
+            const float m_fin = (m == -INFINITY) ? 0.f : m;
+            const size_t lrow = VARLEN ? (size_t)(bh % args.H) * args.total_q + q_tok + i : (size_t)bh * Nq + i;
+            args.lse[lrow] = (l > 0.f) ? m_fin * 0.69314718055994531f + logf(l) : -INFINITY;
+        }
+        // The stores must have read shared memory before the CTA may exit.
+        if (staged && threadIdx.x == 0) bulk_wait_read();
     }
 
     tc_fence_before();
