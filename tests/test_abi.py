@@ -53,6 +53,8 @@ def test_validation_without_gpu(lib):
     assert f(p, p, p, p, None, 1, 1, 8, 8, 64, 0, float("nan"), 0, None) == -1  # scale NaN
     assert f(p, p, p, p, None, 1, 1, 8, 8, 64, 2, 0.125, 0, None) == -1          # causal = 2
     assert f(p, p, p, p, None, 1, 1, 8, 8, 64, 0, 0.125, 7, None) == -1          # dtype
+    assert f(p, p, p, p, None, 256, 256, 8, 8, 64, 0, 0.125, 0, None) == -1      # B * H past the grid's y limit
+    assert f(p, p, p, p, None, 1 << 16, 1 << 16, 8, 8, 64, 0, 0.125, 0, None) == -1  # B * H past int range
     odd = ctypes.c_void_p((1 << 20) + 8)
     assert f(odd, p, p, p, None, 1, 1, 8, 8, 64, 0, 0.125, 0, None) == -3        # q not 16-byte aligned
     assert f(p, p, p, p, ctypes.c_void_p((1 << 20) + 2), 1, 1, 8, 8, 64, 0, 0.125, 0, None) == -3

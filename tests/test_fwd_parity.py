@@ -97,6 +97,20 @@ def test_b1h32_n32768_d128_bf16_causal_sampled(fa):
     _sampled(fa, "b1h32_n32768_d128_bf16_causal")
 
 
+def test_one_long_sequence_sampled(fa):
+    """N = 131072 (1024 K/V tiles per causal row block at the end), one head, 256 sampled
+    rows each over its full key range."""
+    N, d = 131072, 128
+    q, k, v = attn_inputs.make_qkv(1, 1, N, N, d, "bf16", 39, "cuda")
+    o, lse = fa.fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert fa.get_device_status() == fa.FA_OK
+    pairs = attn_inputs.sample_rows(N, 1, 256, seed=39)
+    o_ref, lse_ref = oracle.sampled_rows(q, k, v, pairs, True, 1 / math.sqrt(d))
+    rows = torch.tensor([p[1] for p in pairs], device=o.device)
+    compare(o[0, 0, rows], o_ref, lse[0, 0, rows], lse_ref, q.dtype, "N131072 causal sampled")
+
+
 def test_constant_v_gives_constant_o(fa):
     q, k, _ = attn_inputs.make_qkv(1, 2, 300, 300, 128, "bf16", 31, "cuda")
     v = torch.full_like(k, 0.8125)
@@ -112,6 +126,21 @@ def test_causal_row0_is_v0(fa):
         assert torch.equal(o[:, :, 0], v[:, :, 0])
         s00 = (q[:, :, 0].double() * k[:, :, 0].double()).sum(-1) / math.sqrt(d)
         assert torch.allclose(lse[:, :, 0].double(), s00, atol=1e-4, rtol=0)
+
+
+def test_most_heads_the_grid_allows(fa):
+    """B * H = 65535 (the largest grid y the launch allows) of three-row problems, every
+    head checked; one head more is refused before any launch."""
+    q, k, v = attn_inputs.make_qkv(1, 65535, 3, 5, 64, "f16", 37, "cuda")
+    for causal in (False, True):
+        o, lse = fa.fwd(q, k, v, causal=causal)
+        torch.cuda.synchronize()
+        assert fa.get_device_status() == fa.FA_OK
+        o_ref, lse_ref = oracle.attention(q, k, v, causal, 1 / math.sqrt(64))
+        compare(o, o_ref, lse, lse_ref, q.dtype, f"65535 heads causal={causal}")
+    q2, k2, v2 = attn_inputs.make_qkv(1, 65536, 1, 1, 64, "f16", 38, "cuda")
+    with pytest.raises(fa.FaError):
+        fa.fwd(q2, k2, v2)
 
 
 def test_causal_never_reads_future_tiles(fa):
