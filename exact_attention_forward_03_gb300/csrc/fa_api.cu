@@ -155,6 +155,19 @@ int check_common(const void *q, const void *k, const void *v, const void *o, con
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Heads whose row blocks the forward's launch order interleaves (FwdArgs::head_group).
+// Only a grid of at most about eight waves (ctas <= 8 x SMs) gains from it (its last
+// wave is then a large share of the launch; measured on GB300: +6 % at B4 H16 N1024
+// causal, and 1-4 % lost on the 27-wave causal B2 H32 N8192 launch and on a packed
+// batch): as many heads as keep their K and V, kv_bytes per head, within about 32 MiB
+// of L2, at most 16 and at most the grid's heads.  1 (the plain order) otherwise.
+int fwd_head_group(double kv_bytes, int heads, long long ctas, int num_sms) {
+    if (ctas > 8LL * num_sms) return 1;
+    int g = kv_bytes > 0 ? (int)(32.0 * 1024 * 1024 / kv_bytes) : 16;
+    g = g < 1 ? 1 : (g > 16 ? 16 : g);
+    return g < heads ? g : heads;
+}
+
 int auto_splits(int num_sms, long long rows, int Nk) {
     // About 48 CTAs per SM, at least one 64-key tile per split, at most 64 splits.
     // Measured on GB300 at B=32, H=32, Nk=16384, d=128 (GB/s of compulsory bytes by
@@ -230,6 +243,7 @@ int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
     a.num_m = num_m;
     a.H = H;
     a.group = group;
+    a.head_group = fwd_head_group(4.0 * Nk * d / group, BH, (long long)num_m * BH, st->num_sms);
     a.cu_q = nullptr;
     a.cu_k = nullptr;
     a.total_q = 0;
@@ -374,6 +388,7 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *l
     a.num_m = (max_seqlen_q + kFwdBr - 1) / kFwdBr;
     a.H = H;
     a.group = H / H_kv;
+    a.head_group = 1;
     a.cu_q = cu_seqlens_q;
     a.cu_k = cu_seqlens_k;
     a.total_q = total_q;
@@ -421,6 +436,7 @@ int fa_fwd_varlen_ws(const void *q, const void *k, const void *v, void *o, float
     a.num_m = (int)capacity;
     a.H = H;
     a.group = H / H_kv;
+    a.head_group = 1;
     a.cu_q = cu_seqlens_q;
     a.cu_k = cu_seqlens_k;
     a.total_q = total_q;

@@ -247,7 +247,7 @@ __device__ __noinline__ void rescale_o(uint32_t o_addr, float alpha) {
     }
 }
 
-// VARLEN: packed variable-length batch.  blockIdx.y = sequence * H + head, q, o
+// VARLEN: packed variable-length batch.  by = sequence * H + head, q, o
 // are [total_q, H, d], k, v are [total_k, H_kv, d] (tensor maps indexed by column,
 // head, token), lse is [H, total_q], and sequence s spans tokens
 // [cu_q[s], cu_q[s+1]) of q and [cu_k[s], cu_k[s+1]) of k and v.  A key tile may
@@ -268,21 +268,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Consecutive CTAs take consecutive row blocks of one head, heaviest causal
-    // block first, so the CTAs resident at any time share a few heads' K/V in L2.
-    int bh = blockIdx.y;
+    // Launch order (the hardware hands out CTAs in linear block order): consecutive
+    // CTAs take consecutive row blocks of one head, heaviest causal block first, so the
+    // CTAs resident at any time share a few heads' K/V in L2.  With head_group > 1 (a
+    // grid of a few waves) the (row block, head) pairs are walked head_group heads at a
+    // time instead, and within a group row block by row block across the group's heads,
+    // so that the heaviest blocks of the last heads do not start at the end of the launch.
+    int bx = (int)blockIdx.x, by = (int)blockIdx.y;
+    if (args.head_group > 1) {
+        const int per = (int)gridDim.x, g = args.head_group;
+        const int lin = (int)blockIdx.y * per + (int)blockIdx.x;
+        const int chunk = lin / (g * per), rem = lin - chunk * g * per;
+        const int gh = min(g, (int)gridDim.y - chunk * g);  // heads in this group
+        bx = rem / gh;
+        by = chunk * g + rem % gh;
+    }
+    int bh = by;
     const int causal = args.causal;
     int q0, Nq, Nk, kvh;
     int q_tok = 0, k_tok = 0;  // VARLEN: first token of this sequence in q and in k, v
     if constexpr (VARLEN) {
         int seq, blk = -1;
         if (args.work != nullptr) {
-            // Planned grid: blockIdx.x indexes the work list, blockIdx.y is the head.
-            if ((int)blockIdx.x >= args.work[0]) return;  // past the list (the whole CTA)
-            const int2 w = reinterpret_cast<const int2 *>(args.work + 2)[blockIdx.x];
+            // Planned grid: bx indexes the work list, by is the head.
+            if (bx >= args.work[0]) return;  // past the list (the whole CTA)
+            const int2 w = reinterpret_cast<const int2 *>(args.work + 2)[bx];
             seq = w.x;
             blk = w.y;
-            bh = seq * args.H + (int)blockIdx.y;
+            bh = seq * args.H + by;
         } else {
             seq = bh / args.H;
         }
@@ -292,11 +305,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         Nk = args.cu_k[seq + 1] - k_tok;
         const int num_m = (Nq + kFwdBr - 1) / kFwdBr;
         // Unplanned grid: row blocks past this sequence's own ones hold no row (q0 >= Nq).
-        if (blk < 0) blk = (int)blockIdx.x < num_m ? num_m - 1 - (int)blockIdx.x : -1;
+        if (blk < 0) blk = bx < num_m ? num_m - 1 - bx : -1;
         q0 = blk >= 0 ? blk * kFwdBr : max(Nq, 0);
         kvh = (bh % args.H) / args.group;  // K/V head index within the token's heads
     } else {
-        q0 = (args.num_m - 1 - (int)blockIdx.x) * kFwdBr;
+        q0 = (args.num_m - 1 - bx) * kFwdBr;
         Nq = args.Nq;
         Nk = args.Nk;
         kvh = kv_head(bh, args.H, args.group);  // the K/V head this query head reads

@@ -28,6 +28,9 @@ struct FwdArgs {
     int Nq, Nk;
     int num_m;      // ceil(Nq / (kFwdTilesPerCta * kFwdBr)): row blocks per head
     int H;          // query heads per batch entry
+    // Launch order: CTAs take the row blocks (list entries) of head_group heads at a
+    // time, the heaviest block of each of those heads first (see fa_fwd_kernel).
+    int head_group;
     int group;      // query heads per K/V head (H / H_kv)
     // Variable-length batches (packed [total, heads, d] tensors): per-sequence token
     // offsets, cu_q[s]..cu_q[s+1] and cu_k[s]..cu_k[s+1]; null for dense [B, H, N, d].
