@@ -68,6 +68,14 @@ def test_ragged_shapes(fa, case):
     run_case(fa, B, H, Nq, Nk, d, dtype, causal, seed=7 * Nq + Nk)
 
 
+@pytest.mark.parametrize("B,H", [(1, 17), (3, 11)])
+def test_launch_order_with_a_partial_head_group(fa, B, H):
+    """Grids of a few waves interleave the row blocks of up to 16 heads; with 17 and 33
+    heads the last group holds one head.  Every row is checked."""
+    for causal in (False, True):
+        run_case(fa, B, H, 300, 300, 64, "f16", causal, seed=53 + B * H)
+
+
 def _sampled(fa, wname, count=1024):
     w = attn_inputs.WORKLOADS[wname]
     q, k, v = attn_inputs.make_workload(w, "cuda")
