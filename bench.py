@@ -577,13 +577,34 @@ def run_fa(args, rank, world, local):
         ems = time_calls(ecall, esteps, max(1, min(args.warmup, 3)), None)
         launches += esteps * min(nchunks, w.B * w.kv_heads)
         emean = max_over_ranks(statistics.mean(ems), world)
+        h2d = qh.numel() * qh.element_size() + 2 * kh.numel() * kh.element_size()
+        d2h = oh.numel() * oh.element_size() + lh.numel() * 4
+        # The host link's bound for one step: the same byte counts copied host->device and
+        # device->host at once on two streams, with no compute.
+        lin, lout = torch.empty(h2d, dtype=torch.uint8, device=dev), torch.empty(d2h, dtype=torch.uint8, device=dev)
+        hin = torch.empty(h2d, dtype=torch.uint8, pin_memory=True)
+        hout = torch.empty(d2h, dtype=torch.uint8, pin_memory=True)
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+        def link_step():
+            s_in.wait_stream(torch.cuda.current_stream())
+            s_out.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s_in):
+                lin.copy_(hin, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                hout.copy_(lout, non_blocking=True)
+            torch.cuda.current_stream().wait_stream(s_in)
+            torch.cuda.current_stream().wait_stream(s_out)
+
+        lms = statistics.median(time_calls(link_step, 5, 1, None))
         e2e = {"value": sum_over_ranks(flops, world) / (emean * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": qh.numel() * qh.element_size() + 2 * kh.numel() * kh.element_size(),
-               "d2h_bytes_per_step": oh.numel() * oh.element_size() + lh.numel() * 4,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": emean, "steps": esteps, "entry_point": "fa_fwd_host",
+               "link_bound_ms": lms, "frac_of_link_bound": lms / emean,
                "note": f"host (page-locked) buffers in and out; {nchunks} chunks of heads, copies overlapped with "
-                       "the kernels of the previous chunk"}
-        del ews
+                       "the kernels of the previous chunk; link_bound_ms = the step's host->device and "
+                       "device->host bytes copied at once with no compute"}
+        del ews, lin, lout, hin, hout
 
     # ---- the oracle on this machine's host cores (rank 0, N=1 only)
     cpu = None
