@@ -157,8 +157,8 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Heads whose row blocks the forward's launch order interleaves (FwdArgs::head_group).
 // Only a grid of at most about eight waves (ctas <= 8 x SMs) gains from it (its last
-// wave is then a large share of the launch; measured on GB300: +6 % at B4 H16 N1024
-// causal, and 1-4 % lost on the 27-wave causal B2 H32 N8192 launch and on a packed
+// wave is then a large share of the launch; measured on GB300: +9.6 % at B4 H16 N1024
+// causal, and 1-2 % lost on the 27-wave causal B2 H32 N8192 launch, 1-4 % on a packed
 // batch): as many heads as keep their K and V, kv_bytes per head, within about 32 MiB
 // of L2, at most 16 and at most the grid's heads.  1 (the plain order) otherwise.
 int fwd_head_group(double kv_bytes, int heads, long long ctas, int num_sms) {
