@@ -22,7 +22,7 @@
 //   warp 6     one lane issues S(t) = Q K_t^T for every t
 //   warp 7     idle
 //
-// Tensor memory (512 columns): three score buffers S[0..2] = [0,128),
+// Tensor memory (512 columns; see the paired form below): three score buffers S[0..2] = [0,128),
 // [128,256), [256,384), and O = [384, 384+d).  Tile j's scores go to
 // S[j % 3].  Once a softmax thread holds its row of S(j) in registers it
 // writes P(j) as 16-bit pairs over the first 64 columns of that buffer (and,
@@ -57,6 +57,16 @@
 // row block of a sequence is stored row by row instead, since its box would
 // overlap the next sequence's rows).
 //
+// Paired form (d = 64, grids of a few waves with short rows): two CTAs share an
+// SM.  Each takes 256 tensor-memory columns (one score buffer S[0] = [0,128) and
+// O = [128, 128+d)) and about 81 KB of shared memory (two-slot K and V rings),
+// and is launched at 128 registers per thread; the softmax warpgroup raises its
+// share to 208 and the producer/issuer warpgroup lowers its to 48 (setmaxnreg).
+// With one score buffer S(t+1) waits for PV(t), so each CTA's tiles go
+// S -> softmax -> PV one after another; the other CTA's chain, set-up and
+// epilogue fill the gaps.  The barriers and phases are those of the three-buffer
+// form with the buffer count as the modulus.
+//
 // Every mbarrier wait is bounded (%globaltimer); on expiry the CTA records
 // the timeout in the status word, stops issuing work, waits (bounded) for its
 // in-flight TMA loads and MMAs, frees tensor memory and exits.
@@ -70,15 +80,21 @@ constexpr int kWarpTma = 4, kWarpPv = 5, kWarpS = 6;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kRowSumLimit = 32768.0f;   // 2^15
 
-template <int D>
+// PAIR: two CTAs share an SM (d = 64 only), each with one score buffer and
+// 256 tensor-memory columns; the two CTAs' S -> softmax -> PV chains interleave
+// on the SM, and one CTA's set-up and epilogue overlap the other's tile loop.
+template <int D, bool PAIR = false>
 struct FwdCfg {
     static_assert(D == 64 || D == 128, "head dim");
+    static_assert(!PAIR || D == 64, "two CTAs per SM only at d = 64");
     static constexpr int kBlocks = D / 64;               // 128-byte swizzle blocks per row
     static constexpr int kQBlockBytes = kFwdBr * 128;    // one 64-column block of the Q tile
     static constexpr int kKVBlockBytes = kFwdBc * 128;   // one 64-column block of a K/V tile
     static constexpr int kQBytes = kFwdBr * D * 2;       // the Q tile
     static constexpr int kTileBytes = kFwdBc * D * 2;    // one K or V tile
-    static constexpr int kStages = (D == 128) ? 3 : 6;   // slots per ring (one K ring, one V ring)
+    static constexpr int kStages = PAIR ? 2 : (D == 128) ? 3 : 6;  // slots per ring (one K ring, one V ring)
+    static constexpr int kSBuf = PAIR ? 1 : 3;           // score buffers in tensor memory
+    static constexpr int kAhead = PAIR ? 2 : 3;          // K tiles loaded before the first V tile
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kQBytes;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
@@ -89,9 +105,11 @@ struct FwdCfg {
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-    static constexpr uint32_t kTmemCols = 512;
+    static_assert(!PAIR || 2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
+    static constexpr uint32_t kTmemCols = PAIR ? 256 : 512;
     __device__ static constexpr uint32_t tmem_s(int b) { return 128u * b; }
-    static constexpr uint32_t kTmemO = 384;
+    static constexpr uint32_t kTmemO = 128u * kSBuf;
+    static_assert(kTmemO + D <= kTmemCols, "tensor memory");
 };
 
 // K/V tile j needs element masks when it crosses the ragged end of K or, under
@@ -253,12 +271,18 @@ __device__ __noinline__ void rescale_o(uint32_t o_addr, float alpha) {
 // [cu_q[s], cu_q[s+1]) of q and [cu_k[s], cu_k[s+1]) of k and v.  A key tile may
 // run past its sequence's last key into the next sequence: those keys are masked
 // like the ragged tail of a dense K.  Query rows past the sequence are not stored.
-template <int D, bool BF16, bool VARLEN>
-__global__ void __launch_bounds__(kFwdThreads, 1)
+// Register split of the PAIR form (launched at 128 per thread so that two CTAs fit):
+// the softmax warpgroup takes 208, the producer/issuer warpgroup keeps 48.
+constexpr uint32_t kPairRegsLaunch = 128, kPairRegsSoftmax = 208, kPairRegsIo = 48;
+static_assert(kPairRegsSoftmax + kPairRegsIo <= 2 * kPairRegsLaunch, "register split exceeds the launch");
+
+template <int D, bool BF16, bool VARLEN, bool PAIR = false>
+__global__ void __launch_bounds__(kFwdThreads, PAIR ? 2 : 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const FwdArgs args) {
-    using C = FwdCfg<D>;
+    using C = FwdCfg<D, PAIR>;
+    constexpr int NB = C::kSBuf;
     using PK = Pack<BF16>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -343,7 +367,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // latency overlaps the allocation and the sync.  No other thread touches a
     // barrier before that sync.
     constexpr int kProducer = kWarpTma * 32;
-    const int n_first = min(n, 3);  // K tiles loaded before the sync
+    const int n_first = min(n, C::kAhead);  // K tiles loaded before the sync
     if (threadIdx.x == kProducer) {
         mbar_init(bar(B_QFULL), 1);
         for (int s = 0; s < S_; ++s) {
@@ -396,14 +420,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tmem = *tmem_holder;
     constexpr uint32_t hi = sdesc_hi_sw128(1024);  // 8 rows x 128 B per core group
 
-    if (warp == kWarpTma) {
+    auto producer_role = [&]() {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && n > 0) {
             // The Q tile and K_0 .. K_{n_first-1} went out before the sync (first use of each slot).
             uint32_t pend_k = (1u << n_first) - 1u, pend_v = 0;  // slots with a load issued, per ring
             uint32_t par_k = 0, par_v = 0;                        // phase parity of the last load into each slot
             // Tile `tile` of K (V) goes to slot tile % S of its ring, in the order the two
-            // MMA streams consume them: K_0, K_1, K_2, then V_j, K_{j+3} for j = 0, 1, ...
+            // MMA streams consume them: K_0 .. K_{A-1}, then V_j, K_{j+A} for j = 0, 1, ...
+            // (A = kAhead: 3, or 2 in the paired form).
             auto load = [&](bool is_v, int tile) -> bool {
                 const int s = tile % S_;
                 const uint32_t it = (uint32_t)(tile / S_);
@@ -423,7 +448,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 return true;
             };
             bool ok = true;
-            for (int j = 0; ok && j < n; ++j) ok = load(true, j) && (j + 3 >= n || load(false, j + 3));
+            for (int j = 0; ok && j < n; ++j) ok = load(true, j) && (j + C::kAhead >= n || load(false, j + C::kAhead));
             // Every load issued must land before the CTA may exit.
             volatile int no_abort = 0;
             mbar_wait_bounded(bar(B_QFULL), 0, &no_abort, status);
@@ -432,7 +457,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 if (pend_v & (1u << s)) mbar_wait_bounded(bar(B_VFULL(s)), (par_v >> s) & 1u, &no_abort, status);
             }
         }
-    } else if (warp == kWarpS) {
+    };
+    auto s_issuer_role = [&]() {
         // ------------------------------------------------------------ MMA issuer: S stream
         if (lane == 0 && n > 0) {
             constexpr uint32_t idesc_qk = idesc_f16(128, kFwdBc, BF16, false);
@@ -440,9 +466,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const uint32_t k_lo = sdesc_lo(sb + C::kOffK, 16);
             bool ok = mbar_wait_bounded(bar(B_QFULL), 0, abort_flag, status);
             for (int t = 0; ok && t < n; ++t) {
-                const int b = t % 3, s = t % S_;
-                // S[b] is free once PV(t-3) has read P(t-3) from it.
-                if (t >= 3) ok = mbar_wait_backoff(bar(B_PVDONE(b)), (uint32_t)(t / 3 - 1) & 1u, abort_flag, status, 64);
+                const int b = t % NB, s = t % S_;
+                // S[b] is free once PV(t-NB) has read P(t-NB) from it.
+                if (t >= NB) ok = mbar_wait_backoff(bar(B_PVDONE(b)), (uint32_t)(t / NB - 1) & 1u, abort_flag, status, 64);
                 ok = ok && mbar_wait_backoff(bar(B_KFULL(s)), (uint32_t)(t / S_) & 1u, abort_flag, status, 64);
                 if (!ok) break;
                 tc_fence_after();
@@ -463,7 +489,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             volatile int no_abort = 0;
             mbar_wait_bounded(bar(B_MMAFIN(1)), 0, &no_abort, status);
         }
-    } else if (warp == kWarpPv) {
+    };
+    auto pv_issuer_role = [&]() {
         // ------------------------------------------------------------ MMA issuer: PV stream
         if (lane == 0 && n > 0) {
             constexpr uint32_t idesc_pv = idesc_f16(128, D, BF16, true);
@@ -471,8 +498,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const uint32_t d_o = tmem + C::kTmemO;
             bool ok = true;
             for (int j = 0; ok && j < n; ++j) {
-                const int b = j % 3, s = j % S_;
-                ok = mbar_wait_backoff(bar(B_PFULL(b)), (uint32_t)(j / 3) & 1u, abort_flag, status, 32) &&
+                const int b = j % NB, s = j % S_;
+                ok = mbar_wait_backoff(bar(B_PFULL(b)), (uint32_t)(j / NB) & 1u, abort_flag, status, 32) &&
                      mbar_wait_backoff(bar(B_VFULL(s)), (uint32_t)(j / S_) & 1u, abort_flag, status, 32);
                 if (!ok) break;
                 tc_fence_after();
@@ -496,7 +523,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             volatile int no_abort = 0;
             mbar_wait_bounded(bar(B_MMAFIN(0)), 0, &no_abort, status);
         }
-    } else if (warp < 4) {
+    };
+    auto softmax_role = [&]() {
         // ------------------------------------------------------------ softmax / correction / epilogue
         const int quarter = warp;  // TMEM lanes [32*quarter, 32*quarter+32) belong to this warp
         const int i = q0 + quarter * 32 + lane;
@@ -508,9 +536,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         float l = 0.f;        // running sum of 2^(scale*log2(e)*s - m)
         bool ok = true;
         for (int j = 0; j < n; ++j) {
-            const int b = j % 3;
+            const int b = j % NB;
             ok = __all_sync(0xffffffffu,
-                            mbar_wait_bounded(bar(B_SFULL(b)), (uint32_t)(j / 3) & 1u, abort_flag, status));
+                            mbar_wait_bounded(bar(B_SFULL(b)), (uint32_t)(j / NB) & 1u, abort_flag, status));
             if (!ok) break;
             tc_fence_after();
             const uint32_t s_addr = lane_base + C::tmem_s(b);
@@ -522,7 +550,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             l = r.l;
             if (r.rescale && j > 0) {
                 // O must hold PV(0..j-1) in full before it is scaled.
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_PVDONE((j - 1) % 3)), (uint32_t)((j - 1) / 3) & 1u,
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_PVDONE((j - 1) % NB)), (uint32_t)((j - 1) / NB) & 1u,
                                                                abort_flag, status));
                 if (!ok) break;
                 tc_fence_after();
@@ -610,6 +638,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         // The stores must have read shared memory before the CTA may exit.
         if (staged && threadIdx.x == 0) bulk_wait_read();
+    };
+    // The roles.  Paired form: the producer/issuer warpgroup (warps 4-7) gives
+    // registers to the softmax warpgroup before either splits into its roles.
+    if constexpr (PAIR) {
+        if (warp >= 4) {
+            regs_decrease<kPairRegsIo>();
+            if (warp == kWarpTma) producer_role();
+            else if (warp == kWarpS) s_issuer_role();
+            else if (warp == kWarpPv) pv_issuer_role();
+        } else {
+            regs_increase<kPairRegsSoftmax>();
+            softmax_role();
+        }
+    } else {
+        if (warp == kWarpTma) producer_role();
+        else if (warp == kWarpS) s_issuer_role();
+        else if (warp == kWarpPv) pv_issuer_role();
+        else if (warp < 4) softmax_role();
     }
 
     tc_fence_before();
@@ -621,13 +667,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
 }
 
-template <int D, bool BF16, bool VARLEN>
+template <int D, bool BF16, bool VARLEN, bool PAIR = false>
 static cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                                 const CUtensorMap &to, const FwdArgs &a, int num_m, int rows_y, cudaStream_t stream) {
-    using C = FwdCfg<D>;
-    auto kern = fa_fwd_kernel<D, BF16, VARLEN>;
+    using C = FwdCfg<D, PAIR>;
+    auto kern = fa_fwd_kernel<D, BF16, VARLEN, PAIR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
+    if (PAIR) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e != cudaSuccess) return e;
+    }
     dim3 grid((unsigned)num_m, (unsigned)rows_y, 1);
     return launch_kernel(kern, grid, dim3(kFwdThreads), C::kSmemBytes, stream, tq, tk, tv, to, a);
 }
@@ -635,7 +685,10 @@ static cudaError_t launch_fwd_t(const CUtensorMap &tq, const CUtensorMap &tk, co
 template <bool VARLEN>
 static cudaError_t launch_fwd_any(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
                                   const CUtensorMap &tv, const CUtensorMap &to, const FwdArgs &a, int rows_y,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, bool pair = false) {
+    if (d == 64 && pair && !VARLEN)
+        return bf16 ? launch_fwd_t<64, true, false, true>(tq, tk, tv, to, a, a.num_m, rows_y, stream)
+                    : launch_fwd_t<64, false, false, true>(tq, tk, tv, to, a, a.num_m, rows_y, stream);
     if (d == 64) return bf16 ? launch_fwd_t<64, true, VARLEN>(tq, tk, tv, to, a, a.num_m, rows_y, stream)
                              : launch_fwd_t<64, false, VARLEN>(tq, tk, tv, to, a, a.num_m, rows_y, stream);
     return bf16 ? launch_fwd_t<128, true, VARLEN>(tq, tk, tv, to, a, a.num_m, rows_y, stream)
@@ -643,8 +696,8 @@ static cudaError_t launch_fwd_any(int d, bool bf16, const CUtensorMap &tq, const
 }
 
 cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &to, const FwdArgs &a, int BH, cudaStream_t stream) {
-    return launch_fwd_any<false>(d, bf16, tq, tk, tv, to, a, BH, stream);
+                       const CUtensorMap &to, const FwdArgs &a, int BH, cudaStream_t stream, bool pair) {
+    return launch_fwd_any<false>(d, bf16, tq, tk, tv, to, a, BH, stream, pair);
 }
 
 cudaError_t launch_fwd_varlen(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,

@@ -123,9 +123,10 @@ struct Fp8FwdArgs {
 
 // Each launcher returns the CUDA error of the launch (cudaSuccess when queued).
 // The fused forward: `to` is O's tensor map (the same boxes as Q's), for the TMA
-// stores of the epilogue.
+// stores of the epilogue.  pair (d = 64 only): the form that runs two CTAs per SM,
+// each with one score buffer (see fwd_pair in the C ABI).
 cudaError_t launch_fwd(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const CUtensorMap &to, const FwdArgs &a, int BH, cudaStream_t stream);
+                       const CUtensorMap &to, const FwdArgs &a, int BH, cudaStream_t stream, bool pair = false);
 // Variable-length form: grid (num_m, num_seqs * H), packed tensor maps (x = column,
 // y = head, z = token), a.cu_q / a.cu_k set.
 cudaError_t launch_fwd_varlen(int d, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,

@@ -7,7 +7,7 @@ import torch
 
 import attn_inputs
 import oracle
-from parity import compare
+from parity import LSE_ABS_TOL, compare, round_to, ulp
 
 pytestmark = pytest.mark.gpu
 
@@ -74,6 +74,69 @@ def test_launch_order_with_a_partial_head_group(fa, B, H):
     heads the last group holds one head.  Every row is checked."""
     for causal in (False, True):
         run_case(fa, B, H, 300, 300, 64, "f16", causal, seed=53 + B * H)
+
+
+# Grids of three to eight waves whose CTAs visit few K/V tiles run the d = 64 forward
+# with two CTAs per SM (one score buffer each, so every tile's S waits for the last
+# PV); on a 152-SM GPU each of these shapes takes that form.
+PAIRED = [
+    # B, H, Nq, Nk, d, dtype, causal
+    (4, 16, 1000, 1000, 64, "f16", True),    # ragged last row and key blocks
+    (4, 16, 1000, 1000, 64, "bf16", False),
+    (2, 16, 2048, 2048, 64, "bf16", True),   # 16 K/V tiles for the last row block
+    (4, 16, 900, 1024, 64, "f16", True),     # Nq < Nk: bottom-right diagonal
+]
+
+
+@pytest.mark.parametrize("case", PAIRED, ids=lambda c: "B{}H{}_q{}_k{}_d{}_{}_{}".format(*c[:6], "c" if c[6] else "nc"))
+def test_two_ctas_per_sm_form(fa, case):
+    B, H, Nq, Nk, d, dtype, causal = case
+    run_case(fa, B, H, Nq, Nk, d, dtype, causal, seed=11 * Nq + Nk)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_two_ctas_per_sm_form_moves_its_max(fa, dtype):
+    """The rescale paths in the two-CTAs-per-SM form (64 heads of N = 1024 at d = 64):
+    on even rows of the first 48 heads the scores jump by ~20 (natural-log units) on
+    K/V tile 5, and on the last 16 heads the keys' scores rise with the key index, so
+    the running max moves on every tile (the magnitudes of the d = 128 edge-case tests
+    above).  The output must equal, bit for bit, that of the one-CTA-per-SM form (the
+    same heads four at a time, a grid too small for the paired form), also at scale
+    1/8 (a jump of ~28).  Against the oracle: f16 within the 2e-3 bound; bf16 within
+    the bound its 16-bit weights allow when a few keys dominate a row, 2^-9 max|v|
+    (each weight rounded once, relative error 2^-9, and l summed from the unrounded
+    weights) plus half an output ulp -- on these rows that can exceed 2e-3 by a little
+    (2.2e-3 seen, in both forms alike)."""
+    B, H, N, d = 1, 64, 1024, 64
+    q, k, v = attn_inputs.make_qkv(B, H, N, N, d, dtype, 43, "cuda")
+    q[:, :48, 0::2, 0] += 15.0
+    k[:, :48, 640:768, 0] += 15.0
+    ramp = torch.linspace(-2.0, 2.0, N, device="cuda")[:, None].expand(N, d)
+    q[:, 48:] = math.sqrt(0.5)
+    k[:, 48:] = ramp.to(q.dtype)
+    for scale in (1 / math.sqrt(128), 0.125):
+        for causal in (False, True):
+            o, lse = fa.fwd(q, k, v, causal=causal, scale=scale)
+            torch.cuda.synchronize()
+            assert fa.get_device_status() == fa.FA_OK
+            for h in range(0, H, 4):
+                hs = slice(h, h + 4)
+                o1, lse1 = fa.fwd(q[:, hs].contiguous(), k[:, hs].contiguous(), v[:, hs].contiguous(),
+                                  causal=causal, scale=scale)
+                assert torch.equal(o1, o[:, hs]) and torch.equal(lse1, lse[:, hs]), (scale, causal, h)
+            if scale < 0.1:
+                o_ref, lse_ref = oracle.attention(q, k, v, causal, scale)
+                what = f"paired form, moving max {dtype} causal={causal}"
+                if dtype == "f16":
+                    compare(o, o_ref, lse, lse_ref, q.dtype, what)
+                else:
+                    og = o.double().cpu().numpy()
+                    o_ref = np.asarray(o_ref, dtype=np.float64).reshape(og.shape)
+                    half_ulp = 0.5 * ulp(round_to(o_ref, q.dtype), q.dtype)
+                    bound = 2.0 ** -9 * v.abs().max().item() + half_ulp + 1e-4
+                    assert (np.abs(og - o_ref) <= bound).all(), what
+                    lerr = np.abs(lse.double().cpu().numpy() - np.asarray(lse_ref).reshape(lse.shape))
+                    assert lerr.max() <= LSE_ABS_TOL, what
 
 
 def _sampled(fa, wname, count=1024):
