@@ -78,14 +78,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 }
 
 // The same wait for threads off the critical path: between polls the thread
-// sleeps about `ns` nanoseconds, leaving the issue slots of its SM sub-partition
-// to the warps that share it.
+// sleeps about `ns` nanoseconds (none when ns is 0), leaving the issue slots of
+// its SM sub-partition to the warps that share it.
 __device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity, volatile int *abort, int *status,
                                                   uint32_t ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t n = 1;; ++n) {
-        __nanosleep(ns);
+        if (ns != 0) __nanosleep(ns);
         if (mbar_try_wait(bar, parity)) return true;
         if ((n & 15u) == 0) {
             if (*abort) return false;

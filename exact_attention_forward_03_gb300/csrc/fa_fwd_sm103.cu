@@ -283,6 +283,12 @@ __global__ void __launch_bounds__(kFwdThreads, PAIR ? 2 : 1)
                   const FwdArgs args) {
     using C = FwdCfg<D, PAIR>;
     constexpr int NB = C::kSBuf;
+    // Sleep between an issuing thread's barrier polls.  The paired form's tiles form
+    // one serial S -> softmax -> PV chain per CTA, so its issuers poll without
+    // sleeping (try_wait itself suspends the thread for a while): a wake-up
+    // that waited out a sleep lengthened every link of the chain (+3-5 % on paired
+    // grids without it; neutral on the one-CTA form, which keeps the sleep).
+    constexpr uint32_t kIssuerSleepNs = PAIR ? 0u : 32u;
     using PK = Pack<BF16>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -468,8 +474,8 @@ __global__ void __launch_bounds__(kFwdThreads, PAIR ? 2 : 1)
             for (int t = 0; ok && t < n; ++t) {
                 const int b = t % NB, s = t % S_;
                 // S[b] is free once PV(t-NB) has read P(t-NB) from it.
-                if (t >= NB) ok = mbar_wait_backoff(bar(B_PVDONE(b)), (uint32_t)(t / NB - 1) & 1u, abort_flag, status, 64);
-                ok = ok && mbar_wait_backoff(bar(B_KFULL(s)), (uint32_t)(t / S_) & 1u, abort_flag, status, 64);
+                if (t >= NB) ok = mbar_wait_backoff(bar(B_PVDONE(b)), (uint32_t)(t / NB - 1) & 1u, abort_flag, status, 2 * kIssuerSleepNs);
+                ok = ok && mbar_wait_backoff(bar(B_KFULL(s)), (uint32_t)(t / S_) & 1u, abort_flag, status, 2 * kIssuerSleepNs);
                 if (!ok) break;
                 tc_fence_after();
                 // S(t) = Q K_t^T: K-major A and B, 16 of the d columns per instruction.
@@ -499,8 +505,8 @@ __global__ void __launch_bounds__(kFwdThreads, PAIR ? 2 : 1)
             bool ok = true;
             for (int j = 0; ok && j < n; ++j) {
                 const int b = j % NB, s = j % S_;
-                ok = mbar_wait_backoff(bar(B_PFULL(b)), (uint32_t)(j / NB) & 1u, abort_flag, status, 32) &&
-                     mbar_wait_backoff(bar(B_VFULL(s)), (uint32_t)(j / S_) & 1u, abort_flag, status, 32);
+                ok = mbar_wait_backoff(bar(B_PFULL(b)), (uint32_t)(j / NB) & 1u, abort_flag, status, kIssuerSleepNs) &&
+                     mbar_wait_backoff(bar(B_VFULL(s)), (uint32_t)(j / S_) & 1u, abort_flag, status, kIssuerSleepNs);
                 if (!ok) break;
                 tc_fence_after();
                 // O += P(j) V_j: P from S[b] (the remainder too on masked tiles), V as an
