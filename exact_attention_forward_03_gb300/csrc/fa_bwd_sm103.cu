@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const size_t vec_row = (size_t)bh * ld_rows + seq_off;
                 // Q and dO rows: (row, head) for dense tensors, (head, token) for packed ones
                 const int qy = VARLEN ? bh : q0, qz = VARLEN ? q_tok + q0 : bh;
-                ok = mbar_wait_backoff(bar(B_QEMPTY(s)), (it & 1u) ^ 1u, abort_flag, status, 32);
+                ok = mbar_wait_bounded(bar(B_QEMPTY(s)), (it & 1u) ^ 1u, abort_flag, status);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(B_QFULL(s)), C::kTileBytes + C::kVecBytes);
                 for (int b = 0; b < C::kBlocks; ++b)
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 bulk_load(vdst + 512, args.dvec + vec_row + q0, 512, bar(B_QFULL(s)));
                 pend_q |= 1u << s;
                 par_q = (par_q & ~(1u << s)) | ((it & 1u) << s);
-                ok = mbar_wait_backoff(bar(B_DOEMPTY(s)), (it & 1u) ^ 1u, abort_flag, status, 32);
+                ok = mbar_wait_bounded(bar(B_DOEMPTY(s)), (it & 1u) ^ 1u, abort_flag, status);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(B_DOFULL(s)), C::kTileBytes);
                 for (int b = 0; b < C::kBlocks; ++b)
@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 umma_commit(bar(B_SFULL));
             };
             bool ok = mbar_wait_bounded(bar(B_KV), 0, abort_flag, status) &&
-                      mbar_wait_backoff(bar(B_QFULL(0)), 0, abort_flag, status, 32);
+                      mbar_wait_bounded(bar(B_QFULL(0)), 0, abort_flag, status);
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const uint32_t ph = (uint32_t)(t / S_) & 1u;
                 const uint32_t pt = (uint32_t)t & 1u, pp = (uint32_t)(t - 1) & 1u;
                 // dP^T(t) = V dO_t^T into [128,256); for d = 128 once dQ^T(t-1) has been read out.
-                ok = mbar_wait_backoff(bar(B_DOFULL(s)), ph, abort_flag, status, 32) &&
+                ok = mbar_wait_bounded(bar(B_DOFULL(s)), ph, abort_flag, status) &&
                      (D != 128 || t == 0 || mbar_wait_bounded(bar(B_DQFREE), pp, abort_flag, status));
                 if (!ok) break;
                 tc_fence_after();
@@ -380,8 +380,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // S^T(t+1) next, so that the elementwise warps can start on P(t+1) while the
                 // tensor core does dK(t) and dQ(t); it overwrites P(t) once dV(t) completed.
                 if (t + 1 < n) {
-                    ok = mbar_wait_backoff(bar(B_QFULL((t + 1) % S_)), (uint32_t)((t + 1) / S_) & 1u, abort_flag,
-                                           status, 32) &&
+                    ok = mbar_wait_bounded(bar(B_QFULL((t + 1) % S_)), (uint32_t)((t + 1) / S_) & 1u, abort_flag,
+                                           status) &&
                          mbar_wait_bounded(bar(B_DVDONE), pt, abort_flag, status);
                     if (!ok) break;
                     tc_fence_after();
