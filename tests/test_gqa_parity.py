@@ -41,6 +41,11 @@ FWD = [
     (2, 6, 3, 128, 128, 64, "bf16", True),
     (1, 16, 4, 520, 200, 128, "bf16", True),   # Nq > Nk: early rows see no key
     (1, 32, 8, 1024, 1024, 128, "bf16", True),
+    # d = 64 grids of a few waves, run two CTAs per SM: causal (the group's heads
+    # mapped to their K/V head in the kernel) and non-causal (the group's rows
+    # merged into one head of 4 x 1000 rows)
+    (4, 16, 4, 1000, 1000, 64, "f16", True),
+    (4, 16, 4, 1000, 1000, 64, "bf16", False),
 ]
 
 
