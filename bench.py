@@ -414,14 +414,14 @@ def run_fa(args, rank, world, local):
                              "note": "fp16 and bf16 share the dense 16-bit tensor rate; peak "
                                      f"{peak_src} bf16 burst"}}
 
-    configs = {}
+    workload_lines = {}
     if not args.no_configs:
         for key, wname in (("cfg1", "tiny_d64_f16"), ("cfg1_causal", "tiny_d64_f16_causal"),
                            ("cfg2", "b4h16_n1024_d64_f16"), ("cfg2_causal", "b4h16_n1024_d64_f16_causal"),
                            ("cfg3_noncausal", "b2h32_n8192_d128_bf16"),
                            ("cfg4", "b1h32_n32768_d128_bf16_causal")):
             if wname != w.name:
-                configs[key] = measure_fwd(wname)
+                workload_lines[key] = measure_fwd(wname)
                 launches += args.steps
 
     # ---- packed variable-length batch (fa_fwd_varlen)
@@ -566,7 +566,7 @@ def run_fa(args, rank, world, local):
         launches += 2 * args.steps
         for sp in (8, 16, 32):  # the split count against the HBM roofline (`decode` is --decode-splits)
             if sp != args.decode_splits:
-                configs[f"decode_s{sp}"] = measure_decode(wdec, splits=sp, inputs=dec_in)
+                workload_lines[f"decode_s{sp}"] = measure_decode(wdec, splits=sp, inputs=dec_in)
                 launches += 2 * args.steps
         del dec_in
         torch.cuda.empty_cache()
@@ -658,7 +658,7 @@ def run_fa(args, rank, world, local):
                      "kernel": "fa_fwd_kernel<128,bf16>", "flops_per_launch": flops},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "decode": decode,
         "decode_gqa": decode_gqa, "varlen": varlen, "varlen_bwd": varlen_bwd, "bwd": bwd, "fp8": fp8,
-        **configs,
+        **workload_lines,
         "wall_s_fwd_timed": wall, "ms_fwd_min": min(ms), "ms_fwd_median": statistics.median(ms),
     }
     if rank == 0:
