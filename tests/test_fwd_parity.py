@@ -269,6 +269,44 @@ def test_scores_jump_on_a_later_unmasked_tile(fa, dtype):
         compare(o, o_ref, lse, lse_ref, q.dtype, f"score jump {dtype} causal={causal}")
 
 
+def test_joint_kv_permutation_leaves_output_unchanged(fa):
+    """Without a mask, attention is invariant to permuting the K and V rows together:
+    the kernel on the permuted keys (which reorders every tile's contents and moves
+    keys across tiles and the ragged tail) matches the oracle of the unpermuted ones."""
+    for d, dtype in ((128, "bf16"), (64, "f16")):
+        q, k, v = attn_inputs.make_qkv(2, 3, 300, 700, d, dtype, 71 + d, "cuda")
+        perm = torch.from_numpy(np.random.default_rng(72).permutation(700)).to("cuda")
+        o, lse = fa.fwd(q, k[:, :, perm].contiguous(), v[:, :, perm].contiguous(), causal=False)
+        torch.cuda.synchronize()
+        assert fa.get_device_status() == fa.FA_OK
+        o_ref, lse_ref = oracle.attention(q, k, v, False, 1 / math.sqrt(d))
+        compare(o, o_ref, lse, lse_ref, q.dtype, f"K/V rows permuted, d={d}")
+
+
+def test_affine_v_moves_output_affinely(fa):
+    """V -> a V + b gives O -> a O + b (the weights sum to 1).  On the GPU: the output
+    for the shifted and scaled values (|O| near b = 1.25, where a bf16 ulp is 2^-7)
+    matches the oracle, and differs from a O + b of the unshifted run by no more than
+    the two runs' tolerances plus the rounding of a v + b to bf16 (half an ulp of
+    a max|v| + b); the LSE does not change."""
+    a, b = 0.5, 1.25
+    q, k, v = attn_inputs.make_qkv(1, 4, 500, 500, 128, "bf16", 73, "cuda")
+    v2 = (a * v.float() + b).to(v.dtype)
+    for causal in (False, True):
+        o, lse = fa.fwd(q, k, v, causal=causal)
+        o2, lse2 = fa.fwd(q, k, v2, causal=causal)
+        torch.cuda.synchronize()
+        o_ref, lse_ref = oracle.attention(q, k, v2, causal, 1 / math.sqrt(128))
+        compare(o2, o_ref, lse2, lse_ref, q.dtype, f"affine V causal={causal}")
+        assert torch.equal(lse, lse2)  # the weights do not depend on V
+        o1, o2d = o.double().cpu().numpy(), o2.double().cpu().numpy()
+        vmax = float(v.abs().max())
+        # each run within max(2e-3, ulp) + ulp/2 of fp64, with ulp <= 2^-6 for |O| < 4
+        u = 2.0 ** -6
+        tol = 1.5 * u * (1 + a) + 2.0 ** -9 * (a * vmax + b)
+        assert np.abs(o2d - (a * o1 + b)).max() <= tol
+
+
 def test_lse_optional(fa):
     q, k, v = attn_inputs.make_qkv(1, 1, 130, 130, 64, "f16", 35, "cuda")
     o1, _ = fa.fwd(q, k, v, causal=True, want_lse=False)
