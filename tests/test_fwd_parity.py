@@ -85,6 +85,7 @@ PAIRED = [
     (4, 16, 1000, 1000, 64, "bf16", False),
     (2, 16, 2048, 2048, 64, "bf16", True),   # 16 K/V tiles for the last row block
     (4, 16, 900, 1024, 64, "f16", True),     # Nq < Nk: bottom-right diagonal
+    (4, 16, 1024, 512, 64, "f16", True),     # Nq > Nk: the first four row blocks see no key
 ]
 
 
