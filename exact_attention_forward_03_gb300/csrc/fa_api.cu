@@ -156,13 +156,16 @@ int check_common(const void *q, const void *k, const void *v, const void *o, con
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Heads whose row blocks the forward's launch order interleaves (FwdArgs::head_group).
-// Only a grid of at most about eight waves (ctas <= 8 x SMs) gains from it (its last
-// wave is then a large share of the launch; measured on GB300: +9.6 % at B4 H16 N1024
-// causal, and 1-2 % lost on the 27-wave causal B2 H32 N8192 launch, 1-4 % on a packed
-// batch): as many heads as keep their K and V, kv_bytes per head, within about 32 MiB
-// of L2, at most 16 and at most the grid's heads.  1 (the plain order) otherwise.
-int fwd_head_group(double kv_bytes, int heads, long long ctas, int num_sms) {
-    if (ctas > 8LL * num_sms) return 1;
+// Only a causal grid of at most about eight waves (ctas <= 8 x SMs) gains from it: its
+// heavy last row blocks then no longer start at the end of the launch (measured on
+// GB300: +9.6 % at B4 H16 N1024 causal, 11-29 % on the same grids run two CTAs per SM;
+// 1-2 % lost on the 27-wave causal B2 H32 N8192 launch, 1-4 % on a packed batch).
+// Without a mask every row block costs the same and the wider K/V working set only
+// costs (B4 H16 N1024: -0.6 % with one CTA per SM, -3.5 % with two).  As many heads as
+// keep their K and V, kv_bytes per head, within about 32 MiB of L2, at most 16 and at
+// most the grid's heads; 1 (the plain order) otherwise.
+int fwd_head_group(double kv_bytes, int heads, long long ctas, int num_sms, int causal) {
+    if (!causal || ctas > 8LL * num_sms) return 1;
     int g = kv_bytes > 0 ? (int)(32.0 * 1024 * 1024 / kv_bytes) : 16;
     g = g < 1 ? 1 : (g > 16 ? 16 : g);
     return g < heads ? g : heads;
@@ -257,7 +260,7 @@ int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
     a.num_m = num_m;
     a.H = H;
     a.group = group;
-    a.head_group = fwd_head_group(4.0 * Nk * d / group, BH, (long long)num_m * BH, st->num_sms);
+    a.head_group = fwd_head_group(4.0 * Nk * d / group, BH, (long long)num_m * BH, st->num_sms, causal);
     a.cu_q = nullptr;
     a.cu_k = nullptr;
     a.total_q = 0;
