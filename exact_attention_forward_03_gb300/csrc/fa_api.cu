@@ -174,15 +174,16 @@ int fwd_head_group(double kv_bytes, int heads, long long ctas, int num_sms, int 
 // Whether the d = 64 forward runs in its two-CTAs-per-SM form (one score buffer per
 // CTA, so each CTA's S -> softmax -> PV chain is serial, but one CTA's set-up, last
 // GEMM and epilogue overlap the other's tile loop).  That pays only where those fixed
-// costs weigh most: grids of three to eight waves whose CTAs visit few K/V tiles.
-// Measured on GB300 (paired vs. one CTA per SM, 50 calls between events): B4 H16 N1024
-// f16 +3.7 % (+7.2 % causal), B4 H32 N1024 +0.8 % (+21 % causal), B2 H16 N2048 causal
-// +15 %, B3 H16 N2048 causal +4.0 %; lost at under two waves (-6 to -19 %), on longer
-// rows (B2 H16 N4096 -17 % non-causal) and on large grids (B2 H32 N8192 -9 % causal,
-// -13 % non-causal).
-bool fwd_pair(int d, int causal, int Nk, long long ctas, int num_sms) {
+// costs weigh most: grids of three to eight waves whose CTAs visit at most 16 K/V
+// tiles.  Measured on GB300 (paired vs. one CTA per SM, 50 calls between events): B4
+// H16 N1024 f16 +3.7 % (+7.2 % causal), B4 H32 N1024 +0.8 % (+21 % causal), B2 H16
+// N2048 causal +15 %, B3 H16 N2048 causal +4.0 % (non-causal +1.8 % once neither form
+// interleaves heads); lost at under two waves (-6 to -19 %), on longer rows (B2 H16
+// N4096 -17 % non-causal) and on large grids (B2 H32 N8192 -9 % causal, -13 %
+// non-causal).
+bool fwd_pair(int d, int Nk, long long ctas, int num_sms) {
     const int tiles = (Nk + kFwdBc - 1) / kFwdBc;
-    return d == 64 && ctas >= 3LL * num_sms && ctas <= 8LL * num_sms && tiles <= (causal ? 16 : 8);
+    return d == 64 && ctas >= 3LL * num_sms && ctas <= 8LL * num_sms && tiles <= 16;
 }
 
 int auto_splits(int num_sms, long long rows, int Nk) {
@@ -268,7 +269,7 @@ int fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
     a.num_seqs = 0;
     a.causal = causal;
     a.scale_log2 = scale * 1.4426950408889634f;
-    const bool pair = fwd_pair(d, causal, Nk, (long long)num_m * BH, st->num_sms);
+    const bool pair = fwd_pair(d, Nk, (long long)num_m * BH, st->num_sms);
     cudaError_t e = launch_fwd(d, bf16, tq, tk, tv, to, a, BH, reinterpret_cast<cudaStream_t>(stream), pair);
     return launch_status("kernel launch", e);
 }

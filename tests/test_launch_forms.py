@@ -62,7 +62,7 @@ def test_few_wave_d64_grid_runs_two_ctas_per_sm(fa, causal):
 @pytest.mark.parametrize("shape", [
     (1, 1, 128, 64, "f16", True),        # one CTA
     (1, 8, 4096, 64, "bf16", True),      # 256 CTAs: under three waves
-    (2, 16, 4096, 64, "bf16", False),    # 32 K/V tiles per CTA without a mask
+    (2, 16, 4096, 64, "bf16", False),    # 32 K/V tiles per CTA
     (4, 16, 1024, 128, "bf16", True),    # d = 128 never pairs
 ])
 def test_other_grids_run_one_cta_per_sm(fa, shape):
